@@ -1,0 +1,121 @@
+"""CPU oracle for dense GEMM -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg (and its ``--impl reference`` arm) may import this package. The CUDA
+library never imports it and shares no code with it.
+
+``gemm_ref`` returns ``C_ref`` and ``S`` (both float64) for a block of rows
+and columns of ``C = A * B^T``:
+
+    C_ref[m, n] = sum_k A(m, k) * B(n, k)      (fp64, ascending k)
+    S[m, n]     = sum_k |A(m, k) * B(n, k)|
+
+as the CuTe DSL Ampere SGEMM example's reference check defines the product
+(``einsum("mk,nk->mn")`` in its ``run()``) and as the CK Tile practice GEMM's
+"Result Verification" checks it with a CPU GEMM. The arithmetic is the plain C
+triple loop in ``gemm_oracle.c``; this module only marshals buffers.
+
+Pins: ``tests/test_oracle.py`` checks this oracle against exact rational
+brute force, closed forms, identity/permutation/linearity/transpose
+invariants and the element decoders against numpy on every bit pattern.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gemm_oracle.c`` into ``liboracle.so`` (plain gcc, -O2)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_gemm.restype = ctypes.c_int
+            lib.oracle_gemm.argtypes = [i64, i64, i64,
+                                        p, i64, ctypes.c_int, ctypes.c_int,
+                                        p, i64, ctypes.c_int, ctypes.c_int,
+                                        p, i64, p, i64, p, p, ctypes.c_int]
+            lib.oracle_f16_to_f64.restype = ctypes.c_double
+            lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_f64.restype = ctypes.c_double
+            lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_f32_to_f64.restype = ctypes.c_double
+            lib.oracle_f32_to_f64.argtypes = [ctypes.c_uint32]
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """Threads the oracle uses by default (online host cores)."""
+    return _load().oracle_num_threads()
+
+
+def decode(bits: int, dtype: str) -> float:
+    """Exact value of one stored element (bits of an f32/f16/bf16)."""
+    lib = _load()
+    if dtype == "f16":
+        return lib.oracle_f16_to_f64(bits)
+    if dtype == "bf16":
+        return lib.oracle_bf16_to_f64(bits)
+    return lib.oracle_f32_to_f64(bits)
+
+
+def _ptr(a):
+    return None if a is None or a.size == 0 else a.ctypes.data
+
+
+def gemm_ref(M: int, N: int, K: int,
+             A: np.ndarray, lda: int, a_major: int, a_dtype: str,
+             B: np.ndarray, ldb: int, b_major: int, b_dtype: str,
+             rows=None, cols=None, threads: int = 0, with_s: bool = True):
+    """(C_ref, S) of shape (len(rows), len(cols)); all rows/cols when None.
+
+    ``A``/``B`` are flat storage arrays (float32, or uint16 bit patterns for
+    f16/bf16) addressed as the C ABI does: A K-major ``A[m*lda+k]``, A M-major
+    ``A[k*lda+m]``, B K-major ``B[n*ldb+k]``, B N-major ``B[k*ldb+n]``.
+    """
+    lib = _load()
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else len(r)
+    nc = N if c is None else len(c)
+    C = np.zeros((nr, nc), dtype=np.float64)
+    S = np.zeros((nr, nc), dtype=np.float64) if with_s else None
+    if nr == 0 or nc == 0:
+        return C, S
+    rc = lib.oracle_gemm(M, N, K,
+                         _ptr(A), lda, a_major, DTYPES[a_dtype],
+                         _ptr(B), ldb, b_major, DTYPES[b_dtype],
+                         None if r is None else r.ctypes.data, nr,
+                         None if c is None else c.ctypes.data, nc,
+                         _ptr(C), _ptr(S) if with_s else None, threads)
+    if rc != 0:
+        raise ValueError(f"oracle_gemm rejected the arguments (status {rc})")
+    return C, S

@@ -1,0 +1,320 @@
+"""Pins for the CPU oracle (CPU only).
+
+The oracle is the plain definition C[m,n] = sum_k A(m,k) B(n,k) (fp64) and
+S[m,n] = sum_k |A(m,k) B(n,k)| -- the product the CuTe DSL Ampere SGEMM
+example checks with einsum("mk,nk->mn") in run(), and the CK Tile practice
+GEMM checks with its CPU reference ("Result Verification"). The pages print no
+GEMM output values, so the oracle is pinned to things other than itself:
+
+* exact rational brute force (``fractions``) on tiny shapes, every major,
+  padded leading dimensions and all three element types, with operands
+  decoded by numpy (not by the oracle's decoders);
+* the oracle's element decoders against numpy on every f16/bf16 bit pattern
+  and on random and special f32 patterns;
+* closed forms: all-ones (C = S = K) and the ramp A(m,k) = m+k,
+  B(n,k) = n-k (C = K m n + (n-m) K(K-1)/2 - (K-1)K(2K-1)/6);
+* identity and permutation operands reproduce / permute the other operand;
+* linearity in A on integer data (exact), the transpose identity
+  C(B, A) = C(A, B)^T, and layout invariance (the same logical matrices in
+  every major and leading dimension give the same bytes);
+* sampled rows/columns equal the same rows/columns of the full product;
+* float64 numpy matmul (a library routine) agrees within fp64 rounding;
+* hand-worked small examples in tests/golden/.
+
+``test_pins_catch_planted_mistakes`` plants plausible mistakes (a dropped
+term, a wrong sign, a transposed operand, a wrong leading dimension, a
+swapped major) in a wrapper around the oracle, on the CPU, and checks that
+each one fails at least one pin.
+"""
+
+from __future__ import annotations
+
+import itertools
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- helpers --
+
+def np_decode(storage: np.ndarray, dtype: str) -> np.ndarray:
+    """float64 values of a storage array, decoded by numpy."""
+    if dtype == "f32":
+        return storage.astype(np.float64)
+    if dtype == "f16":
+        return storage.view(np.float16).astype(np.float64)
+    return (storage.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def logical_from_storage(st, rows, kdim, major, ld, dtype):
+    vals = np_decode(st, dtype)
+    out = np.empty((rows, kdim), dtype=np.float64)
+    for r in range(rows):
+        for k in range(kdim):
+            out[r, k] = vals[r * ld + k] if major == 0 else vals[k * ld + r]
+    return out
+
+
+def make_case(M, N, K, a_major, b_major, dtype, dist="normal", seed=0,
+              lda_pad=0, ldb_pad=0, lo=-5, hi=5):
+    lda = (K if a_major == 0 else M) + lda_pad
+    ldb = (K if b_major == 0 else N) + ldb_pad
+    A = datagen.operand(M, K, major=a_major, ld=lda, dtype=dtype, dist=dist,
+                        seed=seed, stream=0, lo=lo, hi=hi)
+    B = datagen.operand(N, K, major=b_major, ld=ldb, dtype=dtype, dist=dist,
+                        seed=seed, stream=1, lo=lo, hi=hi)
+    return A, lda, B, ldb
+
+
+def run_pins(gemm):
+    """Run every structural pin against ``gemm`` (signature of
+    oracle.gemm_ref). Returns the list of pins that failed."""
+    failed = []
+
+    def check(name, cond):
+        if not cond:
+            failed.append(name)
+
+    # exact brute force on tiny shapes (normal data: rounding matters)
+    for (M, N, K), a_major, b_major, dtype in itertools.product(
+            [(1, 1, 1), (2, 3, 4), (3, 2, 5), (4, 4, 3)], (0, 1), (0, 1),
+            ("f32", "f16", "bf16")):
+        A, lda, B, ldb = make_case(M, N, K, a_major, b_major, dtype, seed=M * 7 + K,
+                                   lda_pad=1, ldb_pad=2)
+        LA = logical_from_storage(A, M, K, a_major, lda, dtype)
+        LB = logical_from_storage(B, N, K, b_major, ldb, dtype)
+        C, S = gemm(M, N, K, A, lda, a_major, dtype, B, ldb, b_major, dtype)
+        if not (np.all(np.isfinite(C)) and np.all(np.isfinite(S))):
+            check(f"brute{(M, N, K, a_major, b_major, dtype)}", False)
+            continue
+        ok = True
+        for m in range(M):
+            for n in range(N):
+                ex = sum((Fraction(float(LA[m, k])) * Fraction(float(LB[n, k]))
+                          for k in range(K)), Fraction(0))
+                ab = sum((abs(Fraction(float(LA[m, k])) * Fraction(float(LB[n, k])))
+                          for k in range(K)), Fraction(0))
+                tol = Fraction(K) * Fraction(2) ** -52 * ab
+                ok &= abs(Fraction(float(C[m, n])) - ex) <= tol
+                ok &= abs(Fraction(float(S[m, n])) - ab) <= tol
+        check(f"brute{(M, N, K, a_major, b_major, dtype)}", ok)
+
+    # integer brute force is exact
+    for a_major, b_major in itertools.product((0, 1), (0, 1)):
+        M, N, K = 3, 4, 6
+        A, lda, B, ldb = make_case(M, N, K, a_major, b_major, "f16", dist="int",
+                                   seed=11, lda_pad=3)
+        LA = logical_from_storage(A, M, K, a_major, lda, "f16")
+        LB = logical_from_storage(B, N, K, b_major, ldb, "f16")
+        C, _ = gemm(M, N, K, A, lda, a_major, "f16", B, ldb, b_major, "f16")
+        ex = np.array([[sum(int(LA[m, k]) * int(LB[n, k]) for k in range(K))
+                        for n in range(N)] for m in range(M)], dtype=np.float64)
+        check(f"int-brute{(a_major, b_major)}", np.array_equal(C, ex))
+
+    # all ones: C = S = K
+    for K in (1, 7, 64):
+        A = np.ones(3 * K, np.float32)
+        B = np.ones(2 * K, np.float32)
+        C, S = gemm(3, 2, K, A, K, 0, "f32", B, K, 0, "f32")
+        check(f"ones{K}", np.all(C == K) and np.all(S == K))
+
+    # ramp closed form
+    for M, N, K in ((4, 5, 6), (9, 3, 17)):
+        A = np.array([[m + k for k in range(K)] for m in range(M)], np.float32).ravel()
+        B = np.array([[n - k for k in range(K)] for n in range(N)], np.float32).ravel()
+        C, _ = gemm(M, N, K, A, K, 0, "f32", B, K, 0, "f32")
+        m, n = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+        closed = K * m * n + (n - m) * K * (K - 1) // 2 - (K - 1) * K * (2 * K - 1) // 6
+        check(f"ramp{(M, N, K)}", np.array_equal(C, closed.astype(np.float64)))
+
+    # identity operands, in both majors
+    for major in (0, 1):
+        M, N = 5, 4
+        eye = np.eye(M, dtype=np.float32)                      # A = I (K = M)
+        Bl = datagen.logical(N, M, dist="int", seed=3)          # N x K logical
+        B = Bl.ravel() if major == 0 else Bl.T.copy().ravel()
+        C, _ = gemm(M, N, M, eye.ravel(), M, 0, "f32", B, M if major == 0 else N, major, "f32")
+        check(f"identity-A{major}", np.array_equal(C, Bl.T.astype(np.float64)))
+        Al = datagen.logical(M, N, dist="int", seed=4)          # B = I (K = N)
+        A = Al.ravel() if major == 0 else Al.T.copy().ravel()
+        C, _ = gemm(M, N, N, A, N if major == 0 else M, major, "f32",
+                    np.eye(N, dtype=np.float32).ravel(), N, 0, "f32")
+        check(f"identity-B{major}", np.array_equal(C, Al.astype(np.float64)))
+
+    # permutation: A = P (row m has its one at column pi(m)) -> C[m,n] = B(n, pi(m))
+    rng = np.random.default_rng(5)
+    pi = rng.permutation(6)
+    P = np.zeros((6, 6), np.float32)
+    P[np.arange(6), pi] = 1
+    Bl = datagen.logical(4, 6, dist="int", seed=6)
+    C, _ = gemm(6, 4, 6, P.ravel(), 6, 0, "f32", Bl.ravel(), 6, 0, "f32")
+    check("permutation", np.array_equal(C, Bl[:, pi].T.astype(np.float64)))
+
+    # linearity in A (integer data: exact)
+    M, N, K = 5, 6, 9
+    A1 = datagen.logical(M, K, dist="int", seed=8)
+    A2 = datagen.logical(M, K, dist="int", seed=9)
+    Bl = datagen.logical(N, K, dist="int", seed=10)
+    C1, _ = gemm(M, N, K, A1.ravel(), K, 0, "f32", Bl.ravel(), K, 0, "f32")
+    C2, _ = gemm(M, N, K, A2.ravel(), K, 0, "f32", Bl.ravel(), K, 0, "f32")
+    C12, _ = gemm(M, N, K, (A1 + A2).ravel(), K, 0, "f32", Bl.ravel(), K, 0, "f32")
+    check("linearity", np.array_equal(C12, C1 + C2))
+
+    # transpose: C(N,M; B, A) == C(M,N; A, B)^T, and layout invariance
+    M, N, K = 7, 5, 11
+    ref = None
+    for a_major, b_major in itertools.product((0, 1), (0, 1)):
+        A, lda, B, ldb = make_case(M, N, K, a_major, b_major, "bf16", seed=12,
+                                   lda_pad=a_major * 3, ldb_pad=b_major)
+        C, S = gemm(M, N, K, A, lda, a_major, "bf16", B, ldb, b_major, "bf16")
+        Ct, St = gemm(N, M, K, B, ldb, b_major, "bf16", A, lda, a_major, "bf16")
+        check(f"transpose{(a_major, b_major)}", np.array_equal(C, Ct.T) and np.array_equal(S, St.T))
+        if ref is None:
+            ref = C
+        check(f"layout{(a_major, b_major)}", np.array_equal(C, ref))
+
+    # sampled rows / columns equal the full product
+    M, N, K = 13, 11, 9
+    A, lda, B, ldb = make_case(M, N, K, 1, 0, "f32", seed=13)
+    Cf, Sf = gemm(M, N, K, A, lda, 1, "f32", B, ldb, 0, "f32")
+    rows, cols = np.array([0, 5, 12]), np.array([10, 3])
+    Cr, Sr = gemm(M, N, K, A, lda, 1, "f32", B, ldb, 0, "f32", rows=rows)
+    Cc, _ = gemm(M, N, K, A, lda, 1, "f32", B, ldb, 0, "f32", cols=cols)
+    Cb, _ = gemm(M, N, K, A, lda, 1, "f32", B, ldb, 0, "f32", rows=rows, cols=cols)
+    check("sampled", np.array_equal(Cr, Cf[rows]) and np.array_equal(Sr, Sf[rows])
+          and np.array_equal(Cc, Cf[:, cols]) and np.array_equal(Cb, Cf[np.ix_(rows, cols)]))
+
+    # numpy float64 matmul (library routine) within fp64 rounding
+    M, N, K = 33, 17, 70
+    A, lda, B, ldb = make_case(M, N, K, 0, 1, "f32", dist="pm1", seed=14)
+    C, S = gemm(M, N, K, A, lda, 0, "f32", B, ldb, 1, "f32")
+    LA = A.reshape(M, K).astype(np.float64)
+    LB = B.reshape(K, N).T.astype(np.float64)
+    check("numpy", np.all(np.abs(C - LA @ LB.T) <= K * 2.0 ** -52 * S)
+          and np.allclose(S, np.abs(LA) @ np.abs(LB).T, rtol=1e-14, atol=0))
+    return failed
+
+
+# ------------------------------------------------------------------- tests --
+
+def test_oracle_passes_every_pin():
+    assert run_pins(oracle.gemm_ref) == []
+
+
+def test_decoders_every_16bit_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    with np.errstate(invalid="ignore"):
+        f16 = bits.view(np.float16).astype(np.float64)
+        bf16 = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    for i in range(1 << 16):
+        got16 = oracle.decode(i, "f16")
+        gotbf = oracle.decode(i, "bf16")
+        assert (got16 == f16[i]) or (np.isnan(got16) and np.isnan(f16[i])), hex(i)
+        assert (gotbf == bf16[i]) or (np.isnan(gotbf) and np.isnan(bf16[i])), hex(i)
+
+
+def test_decoder_f32_patterns():
+    rng = np.random.default_rng(0)
+    pats = np.concatenate([rng.integers(0, 1 << 32, 20000, dtype=np.uint64).astype(np.uint32),
+                           np.array([0, 1, 0x007FFFFF, 0x00800000, 0x3F800000, 0x7F7FFFFF,
+                                     0x7F800000, 0x80000001, 0xFF800000], np.uint32)])
+    with np.errstate(invalid="ignore"):
+        ref = pats.view(np.float32).astype(np.float64)
+    for p, r in zip(pats, ref):
+        got = oracle.decode(int(p), "f32")
+        assert got == r or (np.isnan(got) and np.isnan(r)), hex(int(p))
+
+
+def test_golden_examples():
+    """Hand-worked products (values derived by hand in the fixture file)."""
+    with open(os.path.join(GOLDEN, "hand_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    assert cases
+    for case in cases:
+        M, N, K = case["M"], case["N"], case["K"]
+        dt = case["dtype"]
+        A = datagen.to_storage(np.array(case["A"], np.float64).ravel(), dt)
+        B = datagen.to_storage(np.array(case["B"], np.float64).ravel(), dt)
+        C, S = oracle.gemm_ref(M, N, K, A, K, 0, dt, B, K, 0, dt)
+        assert np.array_equal(C, np.array(case["C"], np.float64)), case["name"]
+        assert np.array_equal(S, np.array(case["S"], np.float64)), case["name"]
+
+
+def test_integer_workloads_are_exact_in_fp32():
+    """The integer configurations keep |C| below 2**24 (so float32(C_ref) is
+    exact, whatever the summation order): |C| <= K * max|a| * max|b|."""
+    assert 256 * 5 * 5 < 2 ** 24          # 1024 x 512 x 256, values in [-5, 5]
+    assert 1037 * 3 * 3 < 2 ** 24         # 4095 x 3071 x 1037, values in [-3, 3]
+    assert 8192 * 3 * 3 < 2 ** 24         # 16384 x 256 x 8192, values in [-3, 3]
+    A, lda, B, ldb = make_case(40, 30, 256, 0, 0, "f16", dist="int", seed=1025)
+    C, _ = oracle.gemm_ref(40, 30, 256, A, lda, 0, "f16", B, ldb, 0, "f16")
+    assert np.array_equal(C, np.floor(C)) and np.abs(C).max() <= 256 * 25
+
+
+def test_rejects_bad_arguments():
+    A = np.ones(4, np.float32)
+    with pytest.raises(ValueError):
+        oracle.gemm_ref(2, 2, 2, A, 1, 0, "f32", A, 2, 0, "f32")   # lda < K
+    with pytest.raises(ValueError):
+        oracle.gemm_ref(2, 2, 2, A, 2, 0, "f32", A, 2, 0, "f32", rows=[2])
+    C, S = oracle.gemm_ref(0, 3, 2, A, 2, 0, "f32", A, 2, 0, "f32")
+    assert C.shape == (0, 3)
+    C, S = oracle.gemm_ref(2, 2, 0, None, 1, 0, "f32", None, 1, 0, "f32")
+    assert np.all(C == 0) and np.all(S == 0)
+
+
+# ------------------------------------------------- planted-mistake checks --
+
+def _mutant(kind):
+    """A plausible mistake, planted in a wrapper around the oracle."""
+    def g(M, N, K, A, lda, a_major, a_dt, B, ldb, b_major, b_dt, rows=None, cols=None, **kw):
+        if kind == "drop_last_k" and K > 0:
+            return oracle.gemm_ref(M, N, K - 1, A, lda, a_major, a_dt, B, ldb, b_major,
+                                   b_dt, rows=rows, cols=cols, **kw)
+        if kind == "wrong_sign":
+            C, S = oracle.gemm_ref(M, N, K, A, lda, a_major, a_dt, B, ldb, b_major, b_dt,
+                                   rows=rows, cols=cols, **kw)
+            return -C, S
+        if kind == "swap_a_major" and M == K:
+            return oracle.gemm_ref(M, N, K, A, lda, 1 - a_major, a_dt, B, ldb, b_major,
+                                   b_dt, rows=rows, cols=cols, **kw)
+        if kind == "transposed_result" and M == N:
+            C, S = oracle.gemm_ref(M, N, K, A, lda, a_major, a_dt, B, ldb, b_major, b_dt,
+                                   rows=rows, cols=cols, **kw)
+            return C.T, S.T
+        if kind == "ld_ignored":
+            inner_a = K if a_major == 0 else M
+            inner_b = K if b_major == 0 else N
+            if lda != inner_a or ldb != inner_b:
+                # a kernel that assumes packed storage reads the padded buffer
+                return oracle.gemm_ref(M, N, K, A, inner_a, a_major, a_dt, B, inner_b,
+                                       b_major, b_dt, rows=rows, cols=cols, **kw)
+        if kind == "first_term_twice" and K > 1:
+            C, S = oracle.gemm_ref(M, N, K, A, lda, a_major, a_dt, B, ldb, b_major, b_dt,
+                                   rows=rows, cols=cols, **kw)
+            C1, _ = oracle.gemm_ref(M, N, 1, A, lda, a_major, a_dt, B, ldb, b_major, b_dt,
+                                    rows=rows, cols=cols, **kw)
+            return C + C1, S
+        if kind == "no_abs_in_s":
+            C, S = oracle.gemm_ref(M, N, K, A, lda, a_major, a_dt, B, ldb, b_major, b_dt,
+                                   rows=rows, cols=cols, **kw)
+            return C, C.copy()
+        return oracle.gemm_ref(M, N, K, A, lda, a_major, a_dt, B, ldb, b_major, b_dt,
+                               rows=rows, cols=cols, **kw)
+    return g
+
+
+@pytest.mark.parametrize("kind", ["drop_last_k", "wrong_sign", "swap_a_major",
+                                  "transposed_result", "ld_ignored", "first_term_twice",
+                                  "no_abs_in_s"])
+def test_pins_catch_planted_mistakes(kind):
+    with np.errstate(all="ignore"):
+        assert run_pins(_mutant(kind)), f"no pin caught the planted mistake {kind!r}"
