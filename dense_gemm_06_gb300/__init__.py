@@ -1,0 +1,145 @@
+"""Python binding of libgemm (include/gemm.h): argument marshalling only.
+
+Every function here has the name and the arguments of the C entry point it
+wraps; pointers may be given as integers or as objects with ``data_ptr()``
+(torch tensors), streams as integers, ``torch.cuda.Stream`` objects or None
+(the current torch stream). All work runs in the CUDA kernels of
+``libgemm.so``; there is no other code path: if the library is missing,
+``load()`` raises.
+
+    C[m][n] = sum_k A(m, k) * B(n, k)      (A is M x K, B is N x K)
+
+as in the CuTe DSL Ampere SGEMM example (reference check "mk,nk->mn") and the
+CK Tile practice GEMM. See include/gemm.h for layouts, types and status codes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgemm.so")
+
+# enums of include/gemm.h
+GEMM_MAJOR_K, GEMM_MAJOR_MN = 0, 1
+GEMM_F32, GEMM_F16_F32, GEMM_BF16_F32, GEMM_F16_F16, GEMM_BF16_BF16 = 0, 1, 2, 3, 4
+GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT = \
+    0, -1, -2, -3, -4
+GEMM_OPT_WAIT_LIMIT_NS, GEMM_OPT_TC_CTA_GROUP, GEMM_OPT_TC_FAULT_INJECT = 1, 2, 3
+
+# storage type of A/B and of C per dtype
+IN_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f16", GEMM_BF16_F32: "bf16",
+           GEMM_F16_F16: "f16", GEMM_BF16_BF16: "bf16"}
+OUT_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f32", GEMM_BF16_F32: "f32",
+            GEMM_F16_F16: "f16", GEMM_BF16_BF16: "bf16"}
+
+EXPORTS = ("gemm", "gemm_host", "gemm_strerror", "gemm_check_device_error",
+           "gemm_release_workspace", "gemm_launch_count", "gemm_set_option",
+           "gemm_get_option")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str = "gemm"):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({gemm_strerror(status)})")
+
+
+def load(path: str = LIB_PATH):
+    """Load libgemm.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(
+                f"libgemm.so not found at {path}: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        sig = [i64, i64, i64, vp, i64, ci, vp, i64, ci, vp, i64, ci, ci, vp]
+        for name in ("gemm", "gemm_host"):
+            f = getattr(lib, name)
+            f.restype, f.argtypes = ci, sig
+        lib.gemm_strerror.restype, lib.gemm_strerror.argtypes = ctypes.c_char_p, [ci]
+        lib.gemm_check_device_error.restype = ci
+        lib.gemm_check_device_error.argtypes = [vp]
+        lib.gemm_release_workspace.restype, lib.gemm_release_workspace.argtypes = None, []
+        lib.gemm_launch_count.restype, lib.gemm_launch_count.argtypes = ctypes.c_uint64, []
+        lib.gemm_set_option.restype, lib.gemm_set_option.argtypes = ci, [ci, i64]
+        lib.gemm_get_option.restype, lib.gemm_get_option.argtypes = i64, [ci]
+        _lib = lib
+        return lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    if hasattr(x, "ctypes"):  # numpy array (host buffers for gemm_host)
+        return int(x.ctypes.data)
+    raise TypeError(f"cannot take a pointer of {type(x).__name__}")
+
+
+def _stream(s) -> int:
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return int(torch.cuda.current_stream().cuda_stream)
+        except ImportError:
+            pass
+        return 0
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def gemm(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype, stream=None) -> int:
+    """C = A * B^T on device buffers; returns the gemm_status."""
+    return load().gemm(M, N, K, _ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C), ldc,
+                       c_major, dtype, _stream(stream))
+
+
+def gemm_host(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype,
+              stream=None) -> int:
+    """The same product on host buffers (copies inside, on `stream`)."""
+    return load().gemm_host(M, N, K, _ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C),
+                            ldc, c_major, dtype, _stream(stream))
+
+
+def gemm_strerror(status: int) -> str:
+    return load().gemm_strerror(status).decode()
+
+
+def gemm_check_device_error(stream=None) -> int:
+    return load().gemm_check_device_error(_stream(stream))
+
+
+def gemm_release_workspace() -> None:
+    load().gemm_release_workspace()
+
+
+def gemm_launch_count() -> int:
+    return int(load().gemm_launch_count())
+
+
+def gemm_set_option(option: int, value: int) -> int:
+    return load().gemm_set_option(option, value)
+
+
+def gemm_get_option(option: int) -> int:
+    return int(load().gemm_get_option(option))
+
+
+def check(status: int, where: str = "gemm") -> None:
+    """Raise GemmError for a non-zero status."""
+    if status != GEMM_OK:
+        raise GemmError(status, where)

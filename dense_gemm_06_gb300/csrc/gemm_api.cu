@@ -1,0 +1,417 @@
+// gemm_api.cu -- the C ABI of libgemm (include/gemm.h): argument checks,
+// layout normalisation, kernel selection, scratch memory and error reporting.
+//
+// Argument model after the CuTe DSL Ampere SGEMM example's run() (a_major
+// "k"|"m", b_major "k"|"n", c_major "n"|"m", leading dimension = stride of the
+// non-contiguous mode) and the validation of the Gluon Multi-CTA tutorial's
+// matmul_multicta wrapper (shape and dtype checks before any launch), but
+// reporting status codes instead of raising, and accepting any element-aligned
+// layout.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm.h"
+#include "internal.h"
+
+namespace libgemm {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device error word written by kernels that give up on a wait.
+__device__ unsigned int g_err_word;
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
+std::atomic<int> g_cta_group{0};
+std::atomic<int> g_fault_inject{0};
+
+struct DeviceState {
+    std::once_flag once;
+    int status = kOk;
+    DeviceInfo info{};
+    cudaMemPool_t pool = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+int in_bytes(int dtype) { return dtype == GEMM_F32 ? 4 : 2; }
+int out_bytes(int dtype) { return dtype <= GEMM_BF16_F32 ? 4 : 2; }
+
+// Resolve the current device once: capability check, error word, scratch pool.
+int current_device(DeviceInfo** out, cudaMemPool_t* pool) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return kUnsupported;
+    }
+    if (dev >= kMaxDevices) return kUnsupported;
+    DeviceState& st = g_dev[dev];
+    std::call_once(st.once, [&st, dev] {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+            cudaGetLastError();
+            st.status = kUnsupported;
+            return;
+        }
+        if (prop.major != 10 || prop.minor != 3) {  // built for sm_103a only
+            st.status = kUnsupported;
+            return;
+        }
+        void* err = nullptr;
+        if (cudaGetSymbolAddress(&err, g_err_word) != cudaSuccess) {
+            cudaGetLastError();
+            st.status = kCuda;
+            return;
+        }
+        cudaMemPoolProps pp;
+        std::memset(&pp, 0, sizeof(pp));
+        pp.allocType = cudaMemAllocationTypePinned;
+        pp.location.type = cudaMemLocationTypeDevice;
+        pp.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &pp) != cudaSuccess) {
+            cudaGetLastError();
+            st.status = kCuda;
+            return;
+        }
+        uint64_t keep = ~0ull;  // keep freed scratch cached until released
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        st.pool = pool;
+        st.info.device = dev;
+        st.info.sm_count = prop.multiProcessorCount;
+        st.info.cc_major = prop.major;
+        st.info.cc_minor = prop.minor;
+        st.info.err_word = static_cast<unsigned int*>(err);
+        st.status = kOk;
+    });
+    if (st.status != kOk) return st.status;
+    *out = &st.info;
+    if (pool) *pool = st.pool;
+    return kOk;
+}
+
+bool mul_fits(int64_t a, int64_t b, int64_t limit) { return a == 0 || b <= limit / a; }
+
+// Elements spanned by `outer` rows of `inner` elements, `ld` apart.
+bool span_ok(int64_t outer, int64_t inner, int64_t ld, int esize) {
+    if (outer == 0 || inner == 0) return true;
+    const int64_t lim = INT64_MAX / esize;
+    if (!mul_fits(outer - 1, ld, lim)) return false;
+    return (outer - 1) * ld <= lim - inner;
+}
+
+int64_t span_elems(int64_t outer, int64_t inner, int64_t ld) {
+    return (outer == 0 || inner == 0) ? 0 : (outer - 1) * ld + inner;
+}
+
+// Host-side validation shared by gemm() and gemm_host(). No CUDA calls.
+int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+             const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
+             int dtype) {
+    if (dtype < GEMM_F32 || dtype > GEMM_BF16_BF16) return kInvalidArg;
+    if ((a_major != 0 && a_major != 1) || (b_major != 0 && b_major != 1) ||
+        (c_major != 0 && c_major != 1))
+        return kInvalidArg;
+    if (M < 0 || N < 0 || K < 0) return kInvalidArg;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return kInvalidArg;
+    if (M == 0 || N == 0) return kOk;
+    const int ie = in_bytes(dtype), oe = out_bytes(dtype);
+    // C: N-major (row-major) -> rows M of N; M-major -> rows N of M.
+    const int64_t c_inner = c_major == GEMM_MAJOR_MN ? N : M;
+    const int64_t c_outer = c_major == GEMM_MAJOR_MN ? M : N;
+    if (!C || ldc < c_inner || ldc < 1) return kInvalidArg;
+    if (reinterpret_cast<uintptr_t>(C) % oe) return kInvalidArg;
+    if (!span_ok(c_outer, c_inner, ldc, oe)) return kInvalidArg;
+    if (K == 0) return kOk;
+    const int64_t a_inner = a_major == GEMM_MAJOR_K ? K : M;
+    const int64_t a_outer = a_major == GEMM_MAJOR_K ? M : K;
+    const int64_t b_inner = b_major == GEMM_MAJOR_K ? K : N;
+    const int64_t b_outer = b_major == GEMM_MAJOR_K ? N : K;
+    if (!A || !B) return kInvalidArg;
+    if (lda < a_inner || ldb < b_inner) return kInvalidArg;
+    if (reinterpret_cast<uintptr_t>(A) % ie || reinterpret_cast<uintptr_t>(B) % ie)
+        return kInvalidArg;
+    if (!span_ok(a_outer, a_inner, lda, ie) || !span_ok(b_outer, b_inner, ldb, ie))
+        return kInvalidArg;
+    return kOk;
+}
+
+// ------------------------------------------------------------- helpers --
+
+__global__ void zero_rows_kernel(uint8_t* C, int64_t rows, int64_t row_bytes,
+                                 int64_t pitch_bytes) {
+    const int64_t total = rows * row_bytes;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / row_bytes, c = i - r * row_bytes;
+        C[r * pitch_bytes + c] = 0;
+    }
+}
+
+// Copy `outer` rows of `inner` 16-bit elements (src row pitch `lds`) into dst
+// with row pitch `ldd` (16-byte aligned rows for TMA).
+__global__ void repack16_kernel(const uint16_t* __restrict__ src, int64_t lds,
+                                uint16_t* __restrict__ dst, int64_t ldd, int64_t outer,
+                                int64_t inner) {
+    const int64_t total = outer * inner;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / inner, c = i - r * inner;
+        dst[r * ldd + c] = src[r * lds + c];
+    }
+}
+
+int grid_for(int64_t work, const DeviceInfo& dev) {
+    int64_t blocks = (work + 255) / 256;
+    const int64_t cap = (int64_t)dev.sm_count * 8;
+    if (blocks > cap) blocks = cap;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+int zero_fill(void* C, int64_t rows, int64_t cols, int64_t ld, int esize, const DeviceInfo& dev,
+              cudaStream_t s) {
+    const int64_t rb = cols * esize;
+    zero_rows_kernel<<<grid_for(rows * rb, dev), 256, 0, s>>>(static_cast<uint8_t*>(C), rows,
+                                                               rb, ld * esize);
+    if (cudaGetLastError() != cudaSuccess) return kCuda;
+    note_launch();
+    return kOk;
+}
+
+bool tma_ok(const void* p, int64_t ld, int esize) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ((ld * esize) & 15) == 0;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Normalised problem on the device: column-major C becomes row-major C^T by
+// exchanging the roles of A and B (C^T[n][m] = sum_k B(n,k) A(m,k)).
+Problem normalise(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+                  const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
+                  int dtype) {
+    Problem p;
+    if (c_major == GEMM_MAJOR_MN) {
+        p = {M, N, K, A, lda, a_major == GEMM_MAJOR_K, B, ldb, b_major == GEMM_MAJOR_K, C, ldc,
+             dtype};
+    } else {
+        p = {N, M, K, B, ldb, b_major == GEMM_MAJOR_K, A, lda, a_major == GEMM_MAJOR_K, C, ldc,
+             dtype};
+    }
+    return p;
+}
+
+int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_t s) {
+    if (p.K == 0) return zero_fill(p.C, p.M, p.N, p.ldc, out_bytes(p.dtype), dev, s);
+    if (p.dtype == GEMM_F32) return launch_sgemm_f32(p, dev, s);
+
+    // Tensor-core path: TMA needs 16-byte aligned bases and row pitches.
+    void* scratch[2] = {nullptr, nullptr};
+    int rc = kOk;
+    const void** ops[2] = {&p.A, &p.B};
+    int64_t* lds[2] = {&p.lda, &p.ldb};
+    const bool kmaj[2] = {p.a_kmajor, p.b_kmajor};
+    const int64_t rows[2] = {p.M, p.N};
+    for (int i = 0; i < 2 && rc == kOk; ++i) {
+        if (tma_ok(*ops[i], *lds[i], 2)) continue;
+        const int64_t inner = kmaj[i] ? p.K : rows[i];
+        const int64_t outer = kmaj[i] ? rows[i] : p.K;
+        const int64_t ld2 = round_up(inner, 8);
+        if (cudaMallocFromPoolAsync(&scratch[i], (size_t)(outer * ld2 * 2), pool, s) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            rc = kCuda;
+            break;
+        }
+        repack16_kernel<<<grid_for(outer * inner, dev), 256, 0, s>>>(
+            static_cast<const uint16_t*>(*ops[i]), *lds[i], static_cast<uint16_t*>(scratch[i]),
+            ld2, outer, inner);
+        if (cudaGetLastError() != cudaSuccess) { rc = kCuda; break; }
+        note_launch();
+        *ops[i] = scratch[i];
+        *lds[i] = ld2;
+    }
+    if (rc == kOk)
+        rc = launch_gemm_tc(p, dev, g_cta_group.load(), g_wait_limit_ns.load(),
+                            g_fault_inject.load(), s);
+    for (int i = 0; i < 2; ++i)
+        if (scratch[i]) cudaFreeAsync(scratch[i], s);
+    return rc;
+}
+
+}  // namespace
+
+void note_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace libgemm
+
+using namespace libgemm;
+
+extern "C" {
+
+int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major, const void* B,
+         int64_t ldb, int b_major, void* C, int64_t ldc, int c_major, int dtype, void* stream) {
+    try {
+        int rc = validate(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+        if (rc != kOk) return rc;
+        if (M == 0 || N == 0) return kOk;
+        DeviceInfo* dev = nullptr;
+        cudaMemPool_t pool = nullptr;
+        rc = current_device(&dev, &pool);
+        if (rc != kOk) return rc;
+        const Problem p =
+            normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+        return run_device(p, *dev, pool, static_cast<cudaStream_t>(stream));
+    } catch (...) {
+        return kCuda;
+    }
+}
+
+int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+              const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
+              int dtype, void* stream) {
+    try {
+        int rc = validate(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+        if (rc != kOk) return rc;
+        if (M == 0 || N == 0) return kOk;
+        DeviceInfo* dev = nullptr;
+        cudaMemPool_t pool = nullptr;
+        rc = current_device(&dev, &pool);
+        if (rc != kOk) return rc;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        const int ie = in_bytes(dtype), oe = out_bytes(dtype);
+
+        // Device copies with 16-byte aligned row pitches.
+        const int64_t a_inner = a_major == GEMM_MAJOR_K ? K : M, a_outer = a_major == GEMM_MAJOR_K ? M : K;
+        const int64_t b_inner = b_major == GEMM_MAJOR_K ? K : N, b_outer = b_major == GEMM_MAJOR_K ? N : K;
+        const int64_t c_inner = c_major == GEMM_MAJOR_MN ? N : M, c_outer = c_major == GEMM_MAJOR_MN ? M : N;
+        const int64_t lda_d = round_up(a_inner > 0 ? a_inner : 1, 16 / ie);
+        const int64_t ldb_d = round_up(b_inner > 0 ? b_inner : 1, 16 / ie);
+        const int64_t ldc_d = round_up(c_inner, 16 / oe);
+        const size_t a_bytes = (size_t)(a_outer * lda_d * ie), b_bytes = (size_t)(b_outer * ldb_d * ie);
+        const size_t c_bytes = (size_t)(c_outer * ldc_d * oe);
+
+        void *dA = nullptr, *dB = nullptr, *dC = nullptr;
+        auto release = [&] {
+            if (dA) cudaFreeAsync(dA, s);
+            if (dB) cudaFreeAsync(dB, s);
+            if (dC) cudaFreeAsync(dC, s);
+        };
+        if (cudaMallocFromPoolAsync(&dC, c_bytes, pool, s) != cudaSuccess ||
+            (K > 0 && (cudaMallocFromPoolAsync(&dA, a_bytes, pool, s) != cudaSuccess ||
+                       cudaMallocFromPoolAsync(&dB, b_bytes, pool, s) != cudaSuccess))) {
+            cudaGetLastError();
+            release();
+            return kCuda;
+        }
+        if (K > 0) {
+            if (cudaMemcpy2DAsync(dA, lda_d * ie, A, lda * ie, a_inner * ie, a_outer,
+                                  cudaMemcpyHostToDevice, s) != cudaSuccess ||
+                cudaMemcpy2DAsync(dB, ldb_d * ie, B, ldb * ie, b_inner * ie, b_outer,
+                                  cudaMemcpyHostToDevice, s) != cudaSuccess) {
+                cudaGetLastError();
+                release();
+                return kCuda;
+            }
+        }
+        const Problem p = normalise(M, N, K, dA, lda_d, a_major, dB, ldb_d, b_major, dC, ldc_d,
+                                    c_major, dtype);
+        rc = run_device(p, *dev, pool, s);
+        if (rc == kOk &&
+            cudaMemcpy2DAsync(C, ldc * oe, dC, ldc_d * oe, c_inner * oe, c_outer,
+                              cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+            cudaGetLastError();
+            rc = kCuda;
+        }
+        release();
+        return rc;
+    } catch (...) {
+        return kCuda;
+    }
+}
+
+const char* gemm_strerror(int status) {
+    switch (status) {
+        case GEMM_OK: return "success";
+        case GEMM_ERR_INVALID_ARG:
+            return "invalid argument (size, pointer, leading dimension, enum or alignment)";
+        case GEMM_ERR_UNSUPPORTED: return "no usable device, or the device is not sm_103";
+        case GEMM_ERR_CUDA: return "a CUDA runtime call failed";
+        case GEMM_ERR_TIMEOUT:
+            return "a kernel gave up waiting on a pipeline barrier (time limit exceeded)";
+        default: return "unknown status";
+    }
+}
+
+int gemm_check_device_error(void* stream) {
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev, nullptr);
+    if (rc != kOk) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, dev->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    if (word == kDevErrNone) return kOk;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(dev->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    return kTimeout;
+}
+
+void gemm_release_workspace(void) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (!g_dev[d].pool) continue;
+        if (cudaSetDevice(d) != cudaSuccess) { cudaGetLastError(); continue; }
+        cudaDeviceSynchronize();
+        cudaMemPoolTrimTo(g_dev[d].pool, 0);
+    }
+    cudaSetDevice(cur);
+    cudaGetLastError();
+}
+
+uint64_t gemm_launch_count(void) { return g_launches.load(); }
+
+int gemm_set_option(int option, int64_t value) {
+    switch (option) {
+        case GEMM_OPT_WAIT_LIMIT_NS:
+            if (value < 0) return GEMM_ERR_INVALID_ARG;
+            g_wait_limit_ns.store(value == 0 ? 1000000000ull : (uint64_t)value);
+            return GEMM_OK;
+        case GEMM_OPT_TC_CTA_GROUP:
+            if (value != 0 && value != 1 && value != 2) return GEMM_ERR_INVALID_ARG;
+            g_cta_group.store((int)value);
+            return GEMM_OK;
+        case GEMM_OPT_TC_FAULT_INJECT:
+            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            g_fault_inject.store((int)value);
+            return GEMM_OK;
+        default: return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+int64_t gemm_get_option(int option) {
+    switch (option) {
+        case GEMM_OPT_WAIT_LIMIT_NS: return (int64_t)g_wait_limit_ns.load();
+        case GEMM_OPT_TC_CTA_GROUP: return g_cta_group.load();
+        case GEMM_OPT_TC_FAULT_INJECT: return g_fault_inject.load();
+        default: return -1;
+    }
+}
+
+}  // extern "C"

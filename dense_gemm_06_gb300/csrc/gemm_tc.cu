@@ -1,0 +1,527 @@
+// gemm_tc.cu -- fp16/bf16 GEMM on the 5th-generation tensor cores (tcgen05),
+// C = A * B^T with fp32 accumulation in tensor memory (TMEM).
+//
+// Structure (after the Gluon Multi-CTA tutorial's "fast matmul kernel" and its
+// sections on 2-CTA tcgen05 MMA and TMA in a loop, re-designed for sm_103a in
+// CUDA C++ with hand-written PTX):
+//
+//   * persistent: one CTA per SM (CG == 1) or one CTA pair per two SMs
+//     (CG == 2, a cluster of 2 issuing cta_group::2 MMAs); every CTA walks the
+//     same static tile sequence (cluster c takes tiles c, c + #clusters, ...),
+//     rasterised in bands of BAND tile-rows with the column direction
+//     alternating between bands (a serpentine in the spirit of the tutorial's
+//     planar snake), so concurrently running tiles share A and B panels in L2;
+//   * warp 0 = TMA producer, warp 1 = MMA issuer (+ TMEM allocation), warps
+//     4..7 = epilogue; warps 2..3 idle;
+//   * an STAGES-deep smem ring of (A, B) k-tiles with full/empty mbarriers:
+//     the producer waits `empty`, arms `full` with the expected bytes and
+//     issues TMA loads (128-byte swizzle); the MMA warp waits `full`, issues
+//     BK/16 MMAs and commits to `empty`;
+//   * CG == 2: each CTA loads its own 128 rows of A and its own half of the
+//     256-wide B tile; both CTAs' loads complete on the leader's `full`
+//     barrier (armed by the leader for both), the leader issues M=256 x N=256
+//     MMAs over both CTAs' smem, and its commits are multicast to both CTAs'
+//     `empty` / `acc_full` barriers;
+//   * TMEM holds two 256-column fp32 accumulators (double buffer) so the
+//     epilogue of tile i overlaps the MMAs of tile i+1 (`acc_full` /
+//     `acc_empty` barriers; `acc_empty` lives in the leader and counts the
+//     epilogue warps of both CTAs);
+//   * epilogue: each warp reads its 32 TMEM lanes (= 32 rows of C) in 32-column
+//     chunks with tcgen05.ld, converts (fp32 as is, fp16/bf16 round to nearest
+//     even) and stores straight to global memory, 16-byte vectors where the
+//     row allows and predicated scalars at ragged edges;
+//   * every mbarrier wait is bounded: past `wait_limit_ns` (or once another
+//     wait has failed) the thread records a timeout in the device error word
+//     and its role stops; the CTA drains in-flight copies and MMAs before
+//     releasing TMEM and exiting.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx_sm100.cuh"
+
+namespace libgemm {
+namespace {
+
+using namespace gemm_ptx;
+
+constexpr int BK = 64;           // k per stage: 64 x 16-bit = one 128-byte swizzle row
+constexpr int UMMA_K = 16;       // k per tcgen05.mma (kind::f16)
+constexpr int TILE_N = 256;      // N per tile (per CTA pair when CG == 2)
+constexpr int ROWS_A = 128;      // A rows per CTA (= TMEM lanes)
+constexpr int ACC_COLS = 256;    // TMEM columns per accumulator
+constexpr int TMEM_COLS = 512;   // two accumulators
+constexpr int THREADS = 256;
+constexpr int EPI_WARP0 = 4;     // epilogue warps 4..7 (warp % 4 == TMEM lane quarter)
+constexpr int BAND = 8;          // tile rows per raster band
+
+template <int CG> struct Cfg {
+    static constexpr int B_ROWS = TILE_N / CG;            // B rows (N) held per CTA
+    static constexpr int A_BYTES = ROWS_A * BK * 2;       // 16 KB
+    static constexpr int B_BYTES = B_ROWS * BK * 2;       // 16 KB (CG 2) / 32 KB (CG 1)
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = CG == 2 ? 6 : 4;
+    static constexpr int TILE_M = ROWS_A * CG;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    // barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain, never,
+    // then the TMEM address slot
+    static constexpr int NUM_BARS = 2 * STAGES + 6;
+    static constexpr int BAR_BYTES = NUM_BARS * 8 + 8;
+    static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;  // + alignment slack
+};
+
+struct TcParams {
+    CUtensorMap tmap_a;
+    CUtensorMap tmap_b;
+    void* C;
+    int64_t ldc;
+    int M, N, K;
+    int tiles_m, tiles_n, num_kb;
+    int c_vec;                 // C base / ldc allow 16-byte stores
+    unsigned int* err;         // device error word
+    unsigned long long wait_limit_ns;
+    int fault_inject;          // test hook: 1 = epilogue waits on a barrier nobody arrives at
+};
+
+struct TileCoord {
+    int tm, tn;
+};
+
+__device__ __forceinline__ TileCoord raster(int t, int tiles_m, int tiles_n) {
+    const int band_tiles = BAND * tiles_n;
+    const int band = t / band_tiles;
+    const int within = t - band * band_tiles;
+    const int m_lo = band * BAND;
+    const int rows = min(BAND, tiles_m - m_lo);
+    TileCoord c;
+    c.tm = m_lo + within % rows;
+    c.tn = within / rows;
+    if (band & 1) c.tn = tiles_n - 1 - c.tn;
+    return c;
+}
+
+// Bounded wait: true when the phase completed, false on timeout / abort.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, unsigned int* err,
+                                       unsigned long long limit) {
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++n & 31u) == 0) {
+            if (*reinterpret_cast<volatile unsigned int*>(err) != kDevErrNone) return false;
+            if (globaltimer_ns() - t0 > limit) {
+                atomicCAS(err, kDevErrNone, kDevErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const TcParams& p) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, p.err, p.wait_limit_ns);
+}
+
+// Spin (bounded by time, no barrier) to let in-flight async copies land.
+__device__ __noinline__ void grace_period_ns(uint64_t ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) {
+    }
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_chunk(const TcParams& p, int row, int col,
+                                            const uint32_t (&v)[32]) {
+    if (row >= p.M) return;
+    OutT* crow = static_cast<OutT*>(p.C) + (int64_t)row * p.ldc;
+    if constexpr (sizeof(OutT) == 4) {
+        if (p.c_vec && col + 32 <= p.N) {
+            float4* dst = reinterpret_cast<float4*>(crow + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                     __uint_as_float(v[4 * i + 2]),
+                                     __uint_as_float(v[4 * i + 3]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col + i < p.N) crow[col + i] = __uint_as_float(v[i]);
+        }
+    } else {
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float lo = __uint_as_float(v[2 * i]), hi = __uint_as_float(v[2 * i + 1]);
+            if constexpr (std::is_same<OutT, __nv_bfloat16>::value) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+                packed[i] = *reinterpret_cast<uint32_t*>(&h2);
+            } else {
+                __half2 h2 = __floats2half2_rn(lo, hi);
+                packed[i] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+        }
+        if (p.c_vec && col + 32 <= p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
+        } else {
+            uint16_t* c16 = reinterpret_cast<uint16_t*>(crow);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col + i < p.N)
+                    c16[col + i] = (uint16_t)((packed[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu);
+        }
+    }
+}
+
+template <int CG, bool A_MN, bool B_MN, bool BF16, typename OutT>
+__global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+    using C_ = Cfg<CG>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 128-byte swizzle atoms must sit on 1024-byte boundaries.
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+
+    const uint32_t sA0 = base;
+    const uint32_t sB0 = base + C_::STAGES * C_::A_BYTES;
+    const uint32_t bar0 = base + C_::RING_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C_::STAGES + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * C_::STAGES + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * C_::STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * C_::STAGES + 4);
+    const uint32_t never_bar = bar0 + 8u * (2 * C_::STAGES + 5);  // nothing ever arrives
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::RING_BYTES + 8 * C_::NUM_BARS);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int cluster = CG == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int nclusters = CG == 2 ? (int)num_clusters_x() : (int)gridDim.x;
+    const int total_tiles = p.tiles_m * p.tiles_n;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&p.tmap_a);
+        tma_prefetch_desc(&p.tmap_b);
+        for (int s = 0; s < C_::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);   // leader's producer arms it for both CTAs
+            mbar_init(empty_bar(s), 1);  // one (multicast) MMA commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), CG * 4);  // every epilogue warp of the pair
+        }
+        mbar_init(drain_bar, 1);
+        mbar_init(never_bar, 1);
+        fence_mbarrier_init_cluster();
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before_sync();
+    if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    bool aborted = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
+                const TileCoord tc = raster(t, p.tiles_m, p.tiles_n);
+                const int a_row = tc.tm * C_::TILE_M + (int)rank * ROWS_A;
+                const int b_row = tc.tn * TILE_N + (int)rank * C_::B_ROWS;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(empty_bar(stage), phase ^ 1u, p)) { aborted = true; break; }
+                    const uint32_t fb = CG == 2 ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), CG * C_::STAGE_BYTES);
+                    const uint32_t sa = sA0 + stage * C_::A_BYTES;
+                    const uint32_t sb = sB0 + stage * C_::B_BYTES;
+                    const int k0 = kb * BK;
+                    if constexpr (!A_MN) {
+                        tma_load_2d<CG>(sa, &p.tmap_a, fb, k0, a_row);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < ROWS_A / 64; ++j)
+                            tma_load_2d<CG>(sa + j * 64 * BK * 2, &p.tmap_a, fb, a_row + 64 * j, k0);
+                    }
+                    if constexpr (!B_MN) {
+                        tma_load_2d<CG>(sb, &p.tmap_b, fb, k0, b_row);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C_::B_ROWS / 64; ++j)
+                            tma_load_2d<CG>(sb + j * 64 * BK * 2, &p.tmap_b, fb, b_row + 64 * j, k0);
+                    }
+                    if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (aborted) grace_period_ns(200000);  // let issued copies land
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer --
+        if (leader && lane == 0) {
+            constexpr uint32_t idesc =
+                make_idesc_f16(BF16, A_MN, B_MN, (uint32_t)C_::TILE_M, (uint32_t)TILE_N);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
+                if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, p)) { aborted = true; break; }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(full_bar(stage), phase, p)) { aborted = true; break; }
+                    tc_fence_after_sync();
+                    const uint32_t sa = sA0 + stage * C_::A_BYTES;
+                    const uint32_t sb = sB0 + stage * C_::B_BYTES;
+#pragma unroll
+                    for (int j = 0; j < BK / UMMA_K; ++j) {
+                        // K-major: +32 bytes inside the swizzled 128-byte row;
+                        // MN-major: +16 k-rows of 128 bytes (two 8-row atoms).
+                        const uint64_t ad = A_MN
+                            ? make_sdesc_sw128(sa + j * UMMA_K * 128, 64 * BK * 2, 1024)
+                            : make_sdesc_sw128(sa + j * UMMA_K * 2, 16, 1024);
+                        const uint64_t bd = B_MN
+                            ? make_sdesc_sw128(sb + j * UMMA_K * 128, 64 * BK * 2, 1024)
+                            : make_sdesc_sw128(sb + j * UMMA_K * 2, 16, 1024);
+                        mma_f16<CG>(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                    }
+                    mma_commit<CG>(empty_bar(stage));
+                    if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (aborted) break;
+                mma_commit<CG>(accf_bar(acc));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            // Drain: wait (bounded) until every MMA issued above has completed.
+            if constexpr (CG == 2) mma_commit_pair(drain_bar, (uint16_t)0x1);
+            else mma_commit_local(drain_bar);
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < 1000000000ull) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= EPI_WARP0) {
+        // ------------------------------------------------------ epilogue --
+        const int q = warp - EPI_WARP0;  // TMEM lane quarter of this warp
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        // Every lane waits; the decision to go on is taken warp-uniformly
+        // (__all_sync) because tcgen05.ld below is a .sync.aligned warp op.
+        if (p.fault_inject == 1) {
+            // Test hook: a wait that nothing completes must time out cleanly.
+            if (!__all_sync(0xffffffffu, wait_bar(never_bar, 0u, p))) aborted = true;
+        }
+        for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
+            const TileCoord tc = raster(t, p.tiles_m, p.tiles_n);
+            if (!__all_sync(0xffffffffu, wait_bar(accf_bar(acc), acc_phase, p))) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after_sync();
+            const int row = tc.tm * C_::TILE_M + (int)rank * ROWS_A + q * 32 + lane;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+#pragma unroll 1
+            for (int c = 0; c < ACC_COLS / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
+                tmem_wait_ld();
+                store_chunk<OutT>(p, row, tc.tn * TILE_N + c * 32, v);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+                else mbar_arrive_local(acce_bar(acc));
+            }
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown --
+    tc_fence_before_sync();
+    if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<CG>(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host --
+
+// Signature of the driver's cuTensorMapEncodeTiled (resolved at run time, so
+// the library does not link libcuda directly).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// 2-D map over a 16-bit matrix stored as `outer` rows of `inner` contiguous
+// elements, `ld` elements apart; box {box_inner, box_outer}, 128-byte swizzle,
+// zero fill outside the matrix.
+bool encode_2d(CUtensorMap* map, bool bf16, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                2, const_cast<void*>(ptr), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int CG, bool A_MN, bool B_MN, bool BF16, typename OutT>
+int launch_variant(TcParams& tp, const DeviceInfo& dev, cudaStream_t stream) {
+    using C_ = Cfg<CG>;
+    auto kern = gemm_tc_kernel<CG, A_MN, B_MN, BF16, OutT>;
+    static std::mutex mu;
+    static uint64_t configured = 0;   // bit per device
+    static int max_clusters[64];
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const uint64_t bit = 1ull << (dev.device & 63);
+        if (!(configured & bit)) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C_::SMEM_BYTES) != cudaSuccess)
+                return kCuda;
+            int n = dev.sm_count / CG;
+            if (CG == 2) {
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = CG;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.gridDim = dim3(CG * n);
+                cfg.blockDim = dim3(THREADS);
+                cfg.dynamicSmemBytes = C_::SMEM_BYTES;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int q = 0;
+                if (cudaOccupancyMaxActiveClusters(&q, kern, &cfg) == cudaSuccess && q > 0)
+                    n = q;
+                else
+                    cudaGetLastError();
+            }
+            max_clusters[dev.device & 63] = n;
+            configured |= bit;
+        }
+    }
+    const int total = tp.tiles_m * tp.tiles_n;
+    int nclusters = max_clusters[dev.device & 63];
+    if (nclusters > total) nclusters = total;
+    if (nclusters < 1) nclusters = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(CG * nclusters);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = C_::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tp) != cudaSuccess) return kCuda;
+    note_launch();
+    return kOk;
+}
+
+template <int CG, bool BF16, typename OutT>
+int dispatch_majors(TcParams& tp, bool a_mn, bool b_mn, const DeviceInfo& dev,
+                    cudaStream_t s) {
+    if (!a_mn && !b_mn) return launch_variant<CG, false, false, BF16, OutT>(tp, dev, s);
+    if (!a_mn && b_mn) return launch_variant<CG, false, true, BF16, OutT>(tp, dev, s);
+    if (a_mn && !b_mn) return launch_variant<CG, true, false, BF16, OutT>(tp, dev, s);
+    return launch_variant<CG, true, true, BF16, OutT>(tp, dev, s);
+}
+
+template <int CG>
+int dispatch_types(TcParams& tp, int dtype, bool a_mn, bool b_mn, const DeviceInfo& dev,
+                   cudaStream_t s) {
+    switch (dtype) {
+        case 1: return dispatch_majors<CG, false, float>(tp, a_mn, b_mn, dev, s);
+        case 2: return dispatch_majors<CG, true, float>(tp, a_mn, b_mn, dev, s);
+        case 3: return dispatch_majors<CG, false, __half>(tp, a_mn, b_mn, dev, s);
+        case 4: return dispatch_majors<CG, true, __nv_bfloat16>(tp, a_mn, b_mn, dev, s);
+        default: return kInvalidArg;
+    }
+}
+
+}  // namespace
+
+int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
+                   uint64_t wait_limit_ns, int fault_inject, cudaStream_t stream) {
+    if (!get_encoder()) return kCuda;
+    const int CG = cta_group == 1 ? 1 : 2;
+    const bool bf16 = pr.dtype == 2 || pr.dtype == 4;
+    const int tile_m = ROWS_A * CG;
+    const int b_rows = TILE_N / CG;
+
+    TcParams tp;
+    std::memset(&tp, 0, sizeof(tp));
+    // A: K-major -> dims {K, M}, box {64, 128}; M-major -> dims {M, K}, box {64, 64}.
+    bool ok = pr.a_kmajor
+        ? encode_2d(&tp.tmap_a, bf16, pr.A, pr.K, pr.M, pr.lda, BK, ROWS_A)
+        : encode_2d(&tp.tmap_a, bf16, pr.A, pr.M, pr.K, pr.lda, 64, BK);
+    ok = ok && (pr.b_kmajor
+        ? encode_2d(&tp.tmap_b, bf16, pr.B, pr.K, pr.N, pr.ldb, BK, b_rows)
+        : encode_2d(&tp.tmap_b, bf16, pr.B, pr.N, pr.K, pr.ldb, 64, BK));
+    if (!ok) return kCuda;
+
+    const int out_bytes = pr.dtype <= 2 ? 4 : 2;
+    tp.C = pr.C;
+    tp.ldc = pr.ldc;
+    tp.M = (int)pr.M;
+    tp.N = (int)pr.N;
+    tp.K = (int)pr.K;
+    tp.tiles_m = (int)((pr.M + tile_m - 1) / tile_m);
+    tp.tiles_n = (int)((pr.N + TILE_N - 1) / TILE_N);
+    tp.num_kb = (int)((pr.K + BK - 1) / BK);
+    tp.c_vec = ((reinterpret_cast<uintptr_t>(pr.C) & 15u) == 0 &&
+                ((pr.ldc * out_bytes) & 15) == 0) ? 1 : 0;
+    tp.err = dev.err_word;
+    tp.wait_limit_ns = wait_limit_ns;
+    tp.fault_inject = fault_inject;
+    if ((int64_t)tp.tiles_m * tp.tiles_n > 0x7fffffffLL) return kUnsupported;
+
+    return CG == 1 ? dispatch_types<1>(tp, pr.dtype, !pr.a_kmajor, !pr.b_kmajor, dev, stream)
+                   : dispatch_types<2>(tp, pr.dtype, !pr.a_kmajor, !pr.b_kmajor, dev, stream);
+}
+
+}  // namespace libgemm

@@ -1,0 +1,55 @@
+// internal.h -- interface between the C-ABI layer (gemm_api.cu) and the
+// kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace libgemm {
+
+// A problem after layout normalisation: C is always row-major (N-major) with
+// leading dimension ldc; A is M x K and B is N x K, each K- or MN-major.
+struct Problem {
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    bool a_kmajor;
+    const void* B;
+    int64_t ldb;
+    bool b_kmajor;
+    void* C;
+    int64_t ldc;
+    int dtype;  // gemm_dtype
+};
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int cc_major, cc_minor;
+    unsigned int* err_word;  // device address of this device's error word
+};
+
+// Launchers return 0 or a gemm_status. They enqueue exactly the kernels they
+// report through note_launch().
+int launch_sgemm_f32(const Problem& p, const DeviceInfo& dev, cudaStream_t stream);
+int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, int cta_group,
+                   uint64_t wait_limit_ns, int fault_inject, cudaStream_t stream);
+
+void note_launch(uint64_t n = 1);
+
+// Status codes shared with the public header (kept numerically identical).
+enum : int {
+    kOk = 0,
+    kInvalidArg = -1,
+    kUnsupported = -2,
+    kCuda = -3,
+    kTimeout = -4,
+};
+
+// Codes kernels write into the device error word.
+enum : unsigned int {
+    kDevErrNone = 0,
+    kDevErrTimeout = 1,
+};
+
+}  // namespace libgemm

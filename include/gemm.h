@@ -1,0 +1,183 @@
+/*
+ * gemm.h -- C ABI of libgemm, a dense GEMM for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (every entry point below computes it):
+ *
+ *     C[m][n] = sum_{k=0}^{K-1} A(m,k) * B(n,k),   0 <= m < M, 0 <= n < N
+ *
+ * A is M x K and B is N x K, so C = A * B^T in storage terms. This is the
+ * product of the CuTe DSL Ampere SGEMM example (its module docstring: A is
+ * MxK, B is NxK, C is MxN, each with a selectable major mode; its reference
+ * check contracts "mk,nk->mn") and of the CK Tile practice GEMM ("Problem
+ * Size Configuration": A M x K, B N x K, C M x N). The Gluon Multi-CTA
+ * tutorial's matmul_multicta stores B as K x N row-major, which is the
+ * N-major B here. Accumulation is fp32 for every type; C is overwritten
+ * (beta = 0).
+ *
+ * Layout. Leading dimensions are in ELEMENTS. "major" names the contiguous
+ * dimension (the CuTe SGEMM example's a_major "k"|"m", b_major "k"|"n",
+ * c_major "n"|"m"):
+ *
+ *     A K-major  (GEMM_MAJOR_K)  : A(m,k) = A[m*lda + k],  lda >= K
+ *     A M-major  (GEMM_MAJOR_MN) : A(m,k) = A[k*lda + m],  lda >= M
+ *     B K-major  (GEMM_MAJOR_K)  : B(n,k) = B[n*ldb + k],  ldb >= K
+ *     B N-major  (GEMM_MAJOR_MN) : B(n,k) = B[k*ldb + n],  ldb >= N
+ *     C N-major  (GEMM_MAJOR_MN) : C(m,n) = C[m*ldc + n],  ldc >= N  (row-major)
+ *     C M-major  (GEMM_MAJOR_K)  : C(m,n) = C[n*ldc + m],  ldc >= M  (column-major)
+ *
+ * For C the enum slot GEMM_MAJOR_K means "M contiguous" (C has no K mode).
+ * Any leading dimension and any base address aligned to the element size is
+ * accepted (the pages' kernels need 16-byte aligned contiguous dimensions;
+ * this library repacks misaligned A/B into 16-byte aligned scratch and stores
+ * misaligned C with predicated scalar stores).
+ *
+ * Types (dtype argument):
+ *
+ *     GEMM_F32       A, B, C fp32.       FP32 FFMA (SIMT) kernel.
+ *     GEMM_F16_F32   A, B fp16, C fp32.  tcgen05 tensor-core kernel.
+ *     GEMM_BF16_F32  A, B bf16, C fp32.  tcgen05 tensor-core kernel.
+ *     GEMM_F16_F16   A, B fp16, C fp16.  tcgen05; C rounded to nearest even.
+ *     GEMM_BF16_BF16 A, B bf16, C bf16.  tcgen05; C rounded to nearest even.
+ *
+ * Degenerate sizes: M == 0 or N == 0 is a no-op (returns GEMM_OK, launches
+ * nothing); K == 0 writes C = 0. Negative sizes are GEMM_ERR_INVALID_ARG.
+ *
+ * Execution and ownership: the caller owns A, B and C. gemm() takes DEVICE
+ * pointers of the current device, is asynchronous on `stream` (a
+ * cudaStream_t of the current device; NULL = legacy default stream) and never
+ * synchronises. C overlapping A or B is undefined
+ * and not checked. Scratch for repacking misaligned operands comes from a
+ * library-private, stream-ordered memory pool (cudaMallocAsync on `stream`,
+ * freed on the same stream after use), so concurrent calls on different
+ * streams do not share scratch. C++ exceptions never cross this ABI.
+ *
+ * Errors: every entry point returns GEMM_OK (0) or a negative status:
+ *     GEMM_ERR_INVALID_ARG  bad size, pointer, leading dimension, enum or
+ *                           alignment; checked on the host before any CUDA
+ *                           call, nothing is launched
+ *     GEMM_ERR_UNSUPPORTED  no usable device, or the device is not sm_103
+ *     GEMM_ERR_CUDA         a CUDA runtime call failed (allocation, copy,
+ *                           tensor-map encode, launch)
+ *     GEMM_ERR_TIMEOUT      (from gemm_check_device_error) a kernel gave up
+ *                           waiting on a pipeline barrier after its time
+ *                           limit and wrote no trustworthy C
+ * Device-side timeouts are reported asynchronously: a kernel that times out
+ * records it in a per-device error word and returns; gemm_check_device_error
+ * reads and clears that word. While the word is set, tensor-core kernels on
+ * that device stop at their first wait that does not complete at once, so
+ * results computed between a timeout and the next gemm_check_device_error
+ * are not to be trusted.
+ */
+#ifndef LIBGEMM_GEMM_H
+#define LIBGEMM_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum gemm_major { GEMM_MAJOR_K = 0, GEMM_MAJOR_MN = 1 };
+
+enum gemm_dtype {
+    GEMM_F32 = 0,
+    GEMM_F16_F32 = 1,
+    GEMM_BF16_F32 = 2,
+    GEMM_F16_F16 = 3,
+    GEMM_BF16_BF16 = 4
+};
+
+enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,
+    GEMM_ERR_UNSUPPORTED = -2,
+    GEMM_ERR_CUDA = -3,
+    GEMM_ERR_TIMEOUT = -4
+};
+
+/*
+ * gemm -- C = A * B^T on the current CUDA device, asynchronously on `stream`.
+ * A, B, C are device pointers laid out as described above. The fp32 type runs
+ * the FFMA kernel modelled on the CuTe DSL Ampere SGEMM example (multistage
+ * smem pipeline, register double buffer, predicated tails); the 16-bit types
+ * run the tcgen05 kernel modelled on the Gluon Multi-CTA tutorial's "fast
+ * matmul kernel" (TMA -> mbarrier ring -> 2-CTA tcgen05.mma into TMEM ->
+ * epilogue warps), re-designed for sm_103a.
+ */
+int gemm(int64_t M, int64_t N, int64_t K,
+         const void *A, int64_t lda, int a_major,
+         const void *B, int64_t ldb, int b_major,
+         void *C, int64_t ldc, int c_major,
+         int dtype, void *stream);
+
+/*
+ * gemm_host -- the same product with HOST buffers (pinned or pageable).
+ * On `stream`: takes device buffers from the library's scratch pool (row
+ * pitches rounded up to 16 bytes), copies the addressed elements of A and B
+ * to them (2-D copies, so padding between rows is neither read nor written),
+ * runs the same kernels as gemm(), copies C back into the addressed elements
+ * of the host C and returns the buffers to the pool; the call returns once
+ * the work is enqueued. The host buffers must stay valid and unmodified until
+ * the stream has completed (synchronise before reading C). With pageable host
+ * memory the copies are synchronous with respect to the host. Same status
+ * codes and degenerate-size rules as gemm().
+ */
+int gemm_host(int64_t M, int64_t N, int64_t K,
+              const void *A, int64_t lda, int a_major,
+              const void *B, int64_t ldb, int b_major,
+              void *C, int64_t ldc, int c_major,
+              int dtype, void *stream);
+
+/* gemm_strerror -- a static, NUL-terminated description of a status code. */
+const char *gemm_strerror(int status);
+
+/*
+ * gemm_check_device_error -- synchronises `stream`, then reads and clears the
+ * current device's error word. Returns GEMM_OK, GEMM_ERR_TIMEOUT (a kernel
+ * gave up on a barrier wait) or GEMM_ERR_CUDA (the synchronisation failed).
+ */
+int gemm_check_device_error(void *stream);
+
+/*
+ * gemm_release_workspace -- synchronises every device the library has used
+ * and returns the cached scratch memory of its pools (repack buffers and
+ * gemm_host() copies) to the driver. Call it when no other thread is inside a
+ * gemm* call.
+ */
+void gemm_release_workspace(void);
+
+/*
+ * gemm_launch_count -- number of kernels this library has launched in this
+ * process (all devices). Lets a caller count the launches of a timed region.
+ */
+uint64_t gemm_launch_count(void);
+
+/* Options (process-wide; read at each call). */
+enum gemm_option {
+    /* Time limit of every pipeline barrier wait in the tensor-core kernel, in
+       nanoseconds (default 1000000000; 0 restores the default). A wait that
+       runs past it records GEMM_ERR_TIMEOUT in the device error word and the
+       kernel winds down without further writes to C. */
+    GEMM_OPT_WAIT_LIMIT_NS = 1,
+    /* Tensor-core kernel variant: 0 = automatic (the 2-CTA pair kernel),
+       1 = one CTA per tile (cta_group::1, 128 x 256 tiles),
+       2 = CTA pair per tile (cta_group::2, 256 x 256 tiles). */
+    GEMM_OPT_TC_CTA_GROUP = 2,
+    /* Test hook for the timeout path: 1 makes the tensor-core kernel's
+       epilogue wait on a barrier that nothing completes, so every call times
+       out (after GEMM_OPT_WAIT_LIMIT_NS) and reports GEMM_ERR_TIMEOUT through
+       gemm_check_device_error. 0 (default) = off. */
+    GEMM_OPT_TC_FAULT_INJECT = 3
+};
+
+/* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */
+int gemm_set_option(int option, int64_t value);
+
+/* gemm_get_option -- current value of an option, -1 for an unknown option. */
+int64_t gemm_get_option(int option);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBGEMM_GEMM_H */

@@ -1,0 +1,139 @@
+"""GPU parity on small and ragged shapes, every type, major and kernel variant.
+
+Shapes span several tiles of both kernels (128 x 128 x 16 FFMA tiles,
+128/256 x 256 x 64 tensor-core tiles) and leave ragged tails in M, N and K,
+as the CuTe Ampere SGEMM example's predicated tails and the Gluon Multi-CTA
+tutorial's partial tiles require. Integer-valued inputs are compared
+bit-exactly (fp32 output: C == C_ref; 16-bit output: C == round-to-nearest-
+even(C_ref)); float inputs under |C - C_ref| <= 1e-4 * S (+1 ulp)."""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import datagen
+import dense_gemm_06_gb300 as lg
+from gpu_util import check_full, make_operands, run_device_gemm
+
+pytestmark = pytest.mark.gpu
+
+TC_TYPES = [lg.GEMM_F16_F32, lg.GEMM_BF16_F32, lg.GEMM_F16_F16, lg.GEMM_BF16_BF16]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    lg.load()
+
+
+def rne16(x: np.ndarray, t: str) -> np.ndarray:
+    """Round exact (integer-valued) results to the 16-bit output type."""
+    if t == "f16":
+        return x.astype(np.float16).astype(np.float64)
+    bits = datagen.f32_to_bf16_bits(x.astype(np.float32))
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def run_and_check(M, N, K, dtype, am, bm, cm=1, dist="int", seed=0, lda_pad=0, ldb_pad=0,
+                  ldc_pad=0, cta_group=0):
+    A, lda, B, ldb = make_operands(M, N, K, dtype, am, bm, dist, seed, lda_pad, ldb_pad)
+    C = run_device_gemm(M, N, K, dtype, A, lda, am, B, ldb, bm, cm, ldc_pad, cta_group)
+    what = f"{M}x{N}x{K} dtype={dtype} A{'KM'[am]} B{'KN'[bm]} C{'MN'[cm]} cg={cta_group}"
+    ot = lg.OUT_TYPE[dtype]
+    if dist == "int" and ot != "f32":
+        import oracle
+        it = lg.IN_TYPE[dtype]
+        C_ref, _ = oracle.gemm_ref(M, N, K, A, lda, am, it, B, ldb, bm, it, with_s=False)
+        want = rne16(C_ref, ot)
+        bad = C != want
+        assert not bad.any(), f"{what}: {int(bad.sum())} elements differ from RNE(C_ref)"
+        return
+    check_full(C, M, N, K, dtype, A, lda, am, B, ldb, bm, exact=(dist == "int"), what=what)
+
+
+# ----------------------------------------------------------- FFMA kernel --
+
+SIMT_SHAPES = [(1, 1, 1), (15, 17, 7), (127, 129, 65), (130, 260, 300), (257, 131, 33)]
+
+
+@pytest.mark.parametrize("shape", SIMT_SHAPES)
+@pytest.mark.parametrize("am,bm,cm", list(itertools.product((0, 1), (0, 1), (0, 1))))
+def test_sgemm_ragged(shape, am, bm, cm):
+    M, N, K = shape
+    run_and_check(M, N, K, lg.GEMM_F32, am, bm, cm, dist="pm1", seed=M + N + K)
+
+
+@pytest.mark.parametrize("am,bm", list(itertools.product((0, 1), (0, 1))))
+def test_sgemm_padded_and_unaligned_ld(am, bm):
+    # odd leading dimensions: the MN-major operands take the 4-byte copy path
+    run_and_check(200, 150, 90, lg.GEMM_F32, am, bm, 1, dist="int", seed=3,
+                  lda_pad=3, ldb_pad=5, ldc_pad=1)
+    run_and_check(200, 150, 90, lg.GEMM_F32, am, bm, 0, dist="int", seed=4,
+                  lda_pad=4, ldb_pad=8, ldc_pad=4)
+
+
+# ---------------------------------------------------- tcgen05 kernel --
+
+TC_SHAPES = [(1, 1, 1), (100, 70, 64), (300, 520, 200), (257, 513, 1037)]
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("dtype", TC_TYPES)
+@pytest.mark.parametrize("am,bm", list(itertools.product((0, 1), (0, 1))))
+@pytest.mark.parametrize("shape", TC_SHAPES)
+def test_tc_ragged_integer(shape, am, bm, dtype, cta_group):
+    M, N, K = shape
+    run_and_check(M, N, K, dtype, am, bm, 1, dist="int", seed=K, cta_group=cta_group)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("dtype", TC_TYPES)
+@pytest.mark.parametrize("cm", [0, 1])
+def test_tc_normal_values(dtype, cm, cta_group):
+    run_and_check(384, 520, 640, dtype, 0, 1, cm, dist="normal", seed=5, cta_group=cta_group)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("am,bm", list(itertools.product((0, 1), (0, 1))))
+def test_tc_misaligned_leading_dims(am, bm, cta_group):
+    # leading dimensions that are not 16-byte multiples force the repack path;
+    # an odd ldc forces predicated scalar stores
+    run_and_check(333, 277, 131, lg.GEMM_F16_F32, am, bm, 1, dist="int", seed=6,
+                  lda_pad=1, ldb_pad=3, ldc_pad=1, cta_group=cta_group)
+    run_and_check(333, 277, 131, lg.GEMM_BF16_BF16, am, bm, 0, dist="normal", seed=7,
+                  lda_pad=5, ldb_pad=1, ldc_pad=3, cta_group=cta_group)
+
+
+def test_tc_many_tiles_per_cta():
+    # more tiles than CTA pairs: exercises the TMEM double buffer and the
+    # smem ring phases across tiles
+    run_and_check(2560, 2304, 320, lg.GEMM_F16_F32, 0, 0, 1, dist="int", seed=9)
+    run_and_check(2560, 2304, 320, lg.GEMM_F16_F32, 0, 0, 1, dist="int", seed=9, cta_group=1)
+
+
+# ----------------------------------------------------- degenerate sizes --
+
+@pytest.mark.parametrize("dtype", [lg.GEMM_F32, lg.GEMM_BF16_F32, lg.GEMM_F16_F16])
+def test_k_zero_writes_zero(dtype):
+    C = run_device_gemm(37, 45, 0, dtype, np.zeros(0, np.float32), 1, 0,
+                        np.zeros(0, np.float32), 1, 0, 1, ldc_pad=3)
+    assert np.all(C == 0)
+
+
+@pytest.mark.parametrize("dtype", [lg.GEMM_F32, lg.GEMM_BF16_F32])
+def test_empty_m_or_n_is_a_no_op(dtype):
+    A, lda, B, ldb = make_operands(5, 6, 7, dtype, 0, 0, "int", 1)
+    n0 = lg.gemm_launch_count()
+    C = run_device_gemm(0, 6, 7, dtype, A[:0], lda, 0, B, ldb, 0)
+    assert C.shape == (0, 6)
+    C = run_device_gemm(5, 0, 7, dtype, A, lda, 0, B[:0], ldb, 0)
+    assert C.shape == (5, 0)
+    assert lg.gemm_launch_count() == n0
+
+
+@pytest.mark.parametrize("dtype", [lg.GEMM_F32, lg.GEMM_F16_F32])
+def test_k_one(dtype):
+    run_and_check(129, 257, 1, dtype, 1, 0, 1, dist="int", seed=2)
