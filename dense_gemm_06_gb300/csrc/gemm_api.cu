@@ -30,6 +30,8 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_cta_group{0};
 std::atomic<int> g_fault_inject{0};
+std::atomic<int> g_simt_config{0};
+std::atomic<int> g_simt_transpose{0};
 
 struct DeviceState {
     std::once_flag once;
@@ -205,9 +207,51 @@ Problem normalise(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, i
     return p;
 }
 
+// Whether to give the FFMA kernel an MN-major copy of a K-major operand.
+// The kernel reads MN-major tiles with 16-byte copies and K-major ones with
+// transposing 4-byte copies (about 10% slower at 8192^3); a transpose costs
+// two HBM passes over the operand, 48/n of the GEMM time for the other
+// dimension n, so it pays when n >= 512 and the product is large enough for
+// the extra launch not to matter.
+bool want_transpose(int64_t other_dim, const Problem& p) {
+    const int mode = g_simt_transpose.load();
+    if (mode == 1) return false;
+    if (mode == 2) return true;
+    return other_dim >= 512 && (double)p.M * (double)p.N * (double)p.K >= 2147483648.0;
+}
+
+int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_t s) {
+    void* scratch[2] = {nullptr, nullptr};
+    int rc = kOk;
+    const void** ops[2] = {&p.A, &p.B};
+    int64_t* lds[2] = {&p.lda, &p.ldb};
+    bool* kmaj[2] = {&p.a_kmajor, &p.b_kmajor};
+    const int64_t rows[2] = {p.M, p.N};
+    const int64_t other[2] = {p.N, p.M};
+    for (int i = 0; i < 2 && rc == kOk; ++i) {
+        if (!*kmaj[i] || !want_transpose(other[i], p)) continue;
+        const int64_t ld2 = round_up(rows[i], 4);  // 16-byte rows for vector copies
+        if (cudaMallocFromPoolAsync(&scratch[i], (size_t)(p.K * ld2 * 4), pool, s) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            rc = kCuda;
+            break;
+        }
+        rc = launch_transpose_f32(static_cast<const float*>(*ops[i]), *lds[i],
+                                  static_cast<float*>(scratch[i]), ld2, rows[i], p.K, dev, s);
+        *ops[i] = scratch[i];
+        *lds[i] = ld2;
+        *kmaj[i] = false;
+    }
+    if (rc == kOk) rc = launch_sgemm_f32(p, dev, g_simt_config.load(), s);
+    for (int i = 0; i < 2; ++i)
+        if (scratch[i]) cudaFreeAsync(scratch[i], s);
+    return rc;
+}
+
 int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_t s) {
     if (p.K == 0) return zero_fill(p.C, p.M, p.N, p.ldc, out_bytes(p.dtype), dev, s);
-    if (p.dtype == GEMM_F32) return launch_sgemm_f32(p, dev, s);
+    if (p.dtype == GEMM_F32) return run_sgemm(p, dev, pool, s);
 
     // Tensor-core path: TMA needs 16-byte aligned bases and row pitches.
     void* scratch[2] = {nullptr, nullptr};
@@ -401,6 +445,14 @@ int gemm_set_option(int option, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             g_fault_inject.store((int)value);
             return GEMM_OK;
+        case GEMM_OPT_SIMT_CONFIG:
+            if (value < 0 || value > 6) return GEMM_ERR_INVALID_ARG;
+            g_simt_config.store((int)value);
+            return GEMM_OK;
+        case GEMM_OPT_SIMT_TRANSPOSE:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_simt_transpose.store((int)value);
+            return GEMM_OK;
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -410,6 +462,8 @@ int64_t gemm_get_option(int option) {
         case GEMM_OPT_WAIT_LIMIT_NS: return (int64_t)g_wait_limit_ns.load();
         case GEMM_OPT_TC_CTA_GROUP: return g_cta_group.load();
         case GEMM_OPT_TC_FAULT_INJECT: return g_fault_inject.load();
+        case GEMM_OPT_SIMT_CONFIG: return g_simt_config.load();
+        case GEMM_OPT_SIMT_TRANSPOSE: return g_simt_transpose.load();
         default: return -1;
     }
 }

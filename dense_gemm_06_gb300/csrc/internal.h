@@ -31,7 +31,12 @@ struct DeviceInfo {
 
 // Launchers return 0 or a gemm_status. They enqueue exactly the kernels they
 // report through note_launch().
-int launch_sgemm_f32(const Problem& p, const DeviceInfo& dev, cudaStream_t stream);
+// config: 0 = default tile configuration, 1..4 = a fixed one (see
+// GEMM_OPT_SIMT_CONFIG in gemm.h).
+int launch_sgemm_f32(const Problem& p, const DeviceInfo& dev, int config, cudaStream_t stream);
+// dst[c * ldd + r] = src[r * lds + c] (fp32), rows x cols.
+int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
+                         int64_t cols, const DeviceInfo& dev, cudaStream_t stream);
 int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, int cta_group,
                    uint64_t wait_limit_ns, int fault_inject, cudaStream_t stream);
 

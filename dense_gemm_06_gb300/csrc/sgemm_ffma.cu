@@ -19,6 +19,7 @@
 //     ragged k-tile to the front instead; predicating every copy costs a few
 //     integer compares per k-tile here and keeps one code path);
 //   * predicated epilogue with 128-bit stores when C allows them.
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -28,18 +29,26 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int BK = 16;
-constexpr int STAGES = 4;
 constexpr int THREADS = 256;
 constexpr int PAD = 4;
 constexpr int LDS = BM + PAD;  // floats per k-row in shared memory (BM == BN)
-constexpr int OPERAND_FLOATS = BK * LDS;
-constexpr int STAGE_FLOATS = 2 * OPERAND_FLOATS;
-constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
-constexpr int BAND = 16;  // tile rows per raster band (L2 locality)
+constexpr int BAND = 16;       // tile rows per raster band (L2 locality)
 
 static_assert(BM == BN, "one shared-memory row stride serves both operands");
-static_assert(BK == 16, "the K-major copy mapping below assumes BK == 16");
+
+// Tile configurations (k-depth, ring depth, packed FMA, CTAs/SM). The CuTe Ampere
+// SGEMM example's default is 128 x 128 x 8 with 3 stages.
+template <int BK_, int STAGES_, bool FMA2_, int MINB_>
+struct SgCfg {
+    static constexpr int BK = BK_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr bool FMA2 = FMA2_;
+    static constexpr int MINB = MINB_;  // CTAs per SM the register budget is sized for
+    static constexpr int OPERAND_FLOATS = BK * LDS;
+    static constexpr int STAGE_FLOATS = 2 * OPERAND_FLOATS;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
+    static_assert(BK % 8 == 0 && BK >= 8, "copy mappings assume BK multiple of 8");
+};
 
 struct SgemmParams {
     const float* A;
@@ -75,55 +84,89 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
-// Copy one BK-deep tile of an operand (rows r0.., k0..) into shared memory
-// laid out [k][r] with row stride LDS floats.
-template <bool KMAJOR, int VEC>
-__device__ __forceinline__ void load_tile(uint32_t s, const float* __restrict__ X, int64_t ld,
-                                          int R, int K, int r0, int k0, int tid) {
-    if constexpr (KMAJOR) {
-        // 2048 elements; a warp covers 4 rows x 8 consecutive k (32-byte
-        // segments); smem bank = (4k + r) mod 32 is distinct within the warp.
+// Copies BK-deep tiles of one operand (rows r0 .. r0+127) into shared memory
+// laid out [k][r] with row stride LDS floats. Each thread keeps one pointer
+// that advances by one k-tile per call, a count of the k it has left and a
+// mask of its valid rows, so few registers stay live across the main loop.
+template <int BK, bool KMAJOR, int VEC>
+struct TileLoader {
+    const float* ptr;    // this thread's first element of the next k-tile
+    int64_t ld;
+    int k_left;          // K minus this thread's first k of the next tile
+    int rows_ok;         // K-major: bit q = row q*32 valid; MN 16B: valid rows of
+                         // the vector; MN 4B: 1 if the row is valid
+    uint32_t s_off;      // byte offset of its first element inside a stage
+
+    __device__ __forceinline__ void init(const float* X, int64_t ld_, int R, int K, int r0,
+                                         int tid) {
+        ld = ld_;
+        rows_ok = 0;
+        if constexpr (KMAJOR) {
+            // element e = tid + 256 i: k-group h = e >> 10, row = (e & 1023) >> 3,
+            // k = 8 h + (e & 7); a thread's rows are (tid >> 3) + 32 q.
+            const int rr = tid >> 3, kk = tid & 7;
+            ptr = X + (int64_t)(r0 + rr) * ld + kk;
+            k_left = K - kk;
+            s_off = (uint32_t)(kk * LDS + rr) * 4u;
 #pragma unroll
-        for (int i = 0; i < (BM * BK) / THREADS; ++i) {
-            const int e = tid + i * THREADS;
-            const int h = e >> 10;
-            const int rr = (e & 1023) >> 3;
-            const int kk = (h << 3) | (e & 7);
-            const int gr = r0 + rr, gk = k0 + kk;
-            const bool ok = gr < R && gk < K;
-            const float* src = ok ? X + (int64_t)gr * ld + gk : X;
-            cp_async_4(s + (uint32_t)(kk * LDS + rr) * 4u, src, ok);
-        }
-    } else if constexpr (VEC == 4) {
-        // 512 float4 along r; a warp copies one 512-byte k-row.
-#pragma unroll
-        for (int i = 0; i < (BM * BK) / (4 * THREADS); ++i) {
-            const int idx = tid + i * THREADS;
-            const int kk = idx >> 5;
-            const int rr = (idx & 31) << 2;
-            const int gr = r0 + rr, gk = k0 + kk;
-            int bytes = 0;
-            if (gk < K && gr < R) bytes = (R - gr >= 4 ? 4 : R - gr) * 4;
-            const float* src = bytes ? X + (int64_t)gk * ld + gr : X;
-            cp_async_16(s + (uint32_t)(kk * LDS + rr) * 4u, src, bytes);
-        }
-    } else {
-        // MN-major but not 16-byte aligned: coalesced 4-byte copies along r.
-#pragma unroll
-        for (int i = 0; i < (BM * BK) / THREADS; ++i) {
-            const int e = tid + i * THREADS;
-            const int kk = e >> 7;
-            const int rr = e & 127;
-            const int gr = r0 + rr, gk = k0 + kk;
-            const bool ok = gr < R && gk < K;
-            const float* src = ok ? X + (int64_t)gk * ld + gr : X;
-            cp_async_4(s + (uint32_t)(kk * LDS + rr) * 4u, src, ok);
+            for (int q = 0; q < 4; ++q) rows_ok |= (r0 + rr + 32 * q < R) << q;
+        } else if constexpr (VEC == 4) {
+            // float4 idx = tid + 256 i: k = (tid >> 5) + 8 i, rows 4 (tid & 31) ..
+            const int rr = (tid & 31) << 2, kk = tid >> 5;
+            ptr = X + (int64_t)kk * ld + r0 + rr;
+            k_left = K - kk;
+            s_off = (uint32_t)(kk * LDS + rr) * 4u;
+            const int v = R - (r0 + rr);
+            rows_ok = v >= 4 ? 4 : (v > 0 ? v : 0);
+        } else {
+            // element e = tid + 256 i: k = (tid >> 7) + 2 i, row = tid & 127
+            const int rr = tid & 127, kk = tid >> 7;
+            ptr = X + (int64_t)kk * ld + r0 + rr;
+            k_left = K - kk;
+            s_off = (uint32_t)(kk * LDS + rr) * 4u;
+            rows_ok = (r0 + rr < R) ? 1 : 0;
         }
     }
-}
 
-template <bool A_K, int A_VEC, bool B_K, int B_VEC>
-__global__ void __launch_bounds__(THREADS, 2) sgemm_ffma_kernel(const SgemmParams p) {
+    // Issue the copies of the next k-tile into the stage at byte address s.
+    __device__ __forceinline__ void load_next(uint32_t s) {
+        if constexpr (KMAJOR) {
+            const int64_t ld32 = ld * 32;
+#pragma unroll
+            for (int h = 0; h < BK / 8; ++h) {
+                const bool k_ok = 8 * h < k_left;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const bool ok = k_ok && ((rows_ok >> q) & 1);
+                    cp_async_4(s + s_off + (uint32_t)(8 * h * LDS + 32 * q) * 4u,
+                               ptr + q * ld32 + 8 * h, ok);
+                }
+            }
+            ptr += BK;
+        } else if constexpr (VEC == 4) {
+#pragma unroll
+            for (int i = 0; i < BK / 8; ++i) {
+                const bool ok = rows_ok > 0 && 8 * i < k_left;
+                cp_async_16(s + s_off + (uint32_t)(8 * i * LDS) * 4u, ptr + 8 * i * ld,
+                            ok ? rows_ok * 4 : 0);
+            }
+            ptr += BK * ld;
+        } else {
+#pragma unroll
+            for (int i = 0; i < BK / 2; ++i) {
+                const bool ok = rows_ok && 2 * i < k_left;
+                cp_async_4(s + s_off + (uint32_t)(2 * i * LDS) * 4u, ptr + 2 * i * ld, ok);
+            }
+            ptr += BK * ld;
+        }
+        k_left -= BK;
+    }
+};
+
+template <class Cfg, bool A_K, int A_VEC, bool B_K, int B_VEC>
+__global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const SgemmParams p) {
+    constexpr int BK = Cfg::BK;
+    constexpr int STAGES = Cfg::STAGES;
     extern __shared__ __align__(16) float smem[];
     const int tid = threadIdx.x;
 
@@ -147,57 +190,67 @@ __global__ void __launch_bounds__(THREADS, 2) sgemm_ffma_kernel(const SgemmParam
     const uint32_t s0 = smem_addr(smem);
     const int nkt = (p.K + BK - 1) / BK;
 
-    auto load_stage = [&](int stage, int kt) {
-        const uint32_t sa = s0 + (uint32_t)(stage * STAGE_FLOATS) * 4u;
-        const uint32_t sb = sa + (uint32_t)OPERAND_FLOATS * 4u;
-        load_tile<A_K, A_VEC>(sa, p.A, p.lda, p.M, p.K, m0, kt * BK, tid);
-        load_tile<B_K, B_VEC>(sb, p.B, p.ldb, p.N, p.K, n0, kt * BK, tid);
+    TileLoader<BK, A_K, A_VEC> la;
+    TileLoader<BK, B_K, B_VEC> lb;
+    la.init(p.A, p.lda, p.M, p.K, m0, tid);
+    lb.init(p.B, p.ldb, p.N, p.K, n0, tid);
+    // Tiles are issued strictly in order kt = 0, 1, 2, ...
+    auto load_stage = [&](int stage) {
+        const uint32_t sa = s0 + (uint32_t)(stage * Cfg::STAGE_FLOATS) * 4u;
+        la.load_next(sa);
+        lb.load_next(sa + (uint32_t)Cfg::OPERAND_FLOATS * 4u);
     };
 
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < nkt) load_stage(s, s);
+        if (s < nkt) load_stage(s);
         cp_async_commit();
     }
 
-    float acc[8][8];
+    // acc[i][jj] holds the C columns (2 jj, 2 jj + 1) of b-index space of
+    // row i: packed pairs for the two-lane FMA (fma.rn.f32x2 on sm_100+), or
+    // two scalar FMAs; both round each product-sum once (IEEE fma).
+    float2 acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-    float a[2][8], b[2][8];
+        for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
     for (int kt = 0; kt < nkt; ++kt) {
         cp_async_wait<STAGES - 2>();
         __syncthreads();  // tile kt landed; every thread is done with tile kt-1
 
         const int nt = kt + STAGES - 1;
-        if (nt < nkt) load_stage(nt % STAGES, nt);
+        if (nt < nkt) load_stage(nt % STAGES);
         cp_async_commit();
 
-        const float* sA = smem + (kt % STAGES) * STAGE_FLOATS;
-        const float* sB = sA + OPERAND_FLOATS;
+        const float* sA = smem + (kt % STAGES) * Cfg::STAGE_FLOATS;
+        const float* sB = sA + Cfg::OPERAND_FLOATS;
 
-        auto load_frag = [&](int buf, int k) {
+        // Fully unrolled over the tile's k: the compiler hoists the 128-bit
+        // fragment loads of step k+1 above the FMAs of step k as registers
+        // allow (an explicit second fragment buffer does not fit next to
+        // the 64 accumulators at 2 CTAs/SM).
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
             const float4* pa = reinterpret_cast<const float4*>(sA + k * LDS + ty * 4);
             const float4* pb = reinterpret_cast<const float4*>(sB + k * LDS + tx * 4);
             const float4 a0 = pa[0], a1 = pa[16], b0 = pb[0], b1 = pb[16];
-            a[buf][0] = a0.x; a[buf][1] = a0.y; a[buf][2] = a0.z; a[buf][3] = a0.w;
-            a[buf][4] = a1.x; a[buf][5] = a1.y; a[buf][6] = a1.z; a[buf][7] = a1.w;
-            b[buf][0] = b0.x; b[buf][1] = b0.y; b[buf][2] = b0.z; b[buf][3] = b0.w;
-            b[buf][4] = b1.x; b[buf][5] = b1.y; b[buf][6] = b1.z; b[buf][7] = b1.w;
-        };
-
-        load_frag(0, 0);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float2 b[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                 make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
-        for (int k = 0; k < BK; ++k) {
-            if (k + 1 < BK) load_frag((k + 1) & 1, k + 1);
+            for (int i = 0; i < 8; ++i) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    acc[i][j] = fmaf(a[k & 1][i], b[k & 1][j], acc[i][j]);
+                for (int j = 0; j < 4; ++j) {
+                    if constexpr (Cfg::FMA2) {
+                        acc[i][j] = __ffma2_rn(make_float2(a[i], a[i]), b[j], acc[i][j]);
+                    } else {
+                        acc[i][j].x = fmaf(a[i], b[j].x, acc[i][j].x);
+                        acc[i][j].y = fmaf(a[i], b[j].y, acc[i][j].y);
+                    }
+                }
+            }
         }
     }
     cp_async_wait<0>();
@@ -211,34 +264,86 @@ __global__ void __launch_bounds__(THREADS, 2) sgemm_ffma_kernel(const SgemmParam
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = n0 + tx * 4 + h * 64;
+            const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                                acc[i][2 * h + 1].y};
             if (p.c_vec && col + 3 < p.N) {
-                *reinterpret_cast<float4*>(crow + col) =
-                    make_float4(acc[i][h * 4 + 0], acc[i][h * 4 + 1], acc[i][h * 4 + 2],
-                                acc[i][h * 4 + 3]);
+                *reinterpret_cast<float4*>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (col + j < p.N) crow[col + j] = acc[i][h * 4 + j];
+                    if (col + j < p.N) crow[col + j] = v[j];
             }
         }
     }
 }
 
-template <bool A_K, int A_VEC, bool B_K, int B_VEC>
-int launch_variant(const SgemmParams& sp, cudaStream_t stream) {
-    auto kern = sgemm_ffma_kernel<A_K, A_VEC, B_K, B_VEC>;
-    static bool configured = false;  // attribute is per function, set once
-    if (!configured) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return kCuda;
-        configured = true;
-    }
+// Sets the dynamic shared-memory limit of `kern` once per device; `done` is
+// the calling variant's own flag word (one bit per device).
+template <class Kern>
+bool configure_once(Kern kern, std::atomic<uint64_t>& done, int device, int smem_bytes) {
+    const uint64_t bit = 1ull << (device & 63);
+    if (done.load() & bit) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+        cudaSuccess)
+        return false;
+    done.fetch_or(bit);
+    return true;
+}
+
+template <class Cfg, bool A_K, int A_VEC, bool B_K, int B_VEC>
+int launch_variant(const SgemmParams& sp, int device, cudaStream_t stream) {
+    auto kern = sgemm_ffma_kernel<Cfg, A_K, A_VEC, B_K, B_VEC>;
+    static std::atomic<uint64_t> configured{0};  // per kernel variant
+    if (!configure_once(kern, configured, device, Cfg::SMEM_BYTES)) return kCuda;
     const int64_t tiles = (int64_t)sp.tiles_m * sp.tiles_n;
-    kern<<<dim3((unsigned)tiles), dim3(THREADS), SMEM_BYTES, stream>>>(sp);
+    kern<<<dim3((unsigned)tiles), dim3(THREADS), Cfg::SMEM_BYTES, stream>>>(sp);
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     note_launch();
     return kOk;
+}
+
+template <class Cfg>
+int launch_layout(const SgemmParams& sp, int av, int bv, int device, cudaStream_t s) {
+#define SG_CASE(AV, BV, AK, AVEC, BK_, BVEC) \
+    if (av == AV && bv == BV) return launch_variant<Cfg, AK, AVEC, BK_, BVEC>(sp, device, s);
+    SG_CASE(0, 0, true, 1, true, 1)
+    SG_CASE(0, 4, true, 1, false, 4)
+    SG_CASE(0, 1, true, 1, false, 1)
+    SG_CASE(4, 0, false, 4, true, 1)
+    SG_CASE(4, 4, false, 4, false, 4)
+    SG_CASE(4, 1, false, 4, false, 1)
+    SG_CASE(1, 0, false, 1, true, 1)
+    SG_CASE(1, 4, false, 1, false, 4)
+    SG_CASE(1, 1, false, 1, false, 1)
+#undef SG_CASE
+    return kInvalidArg;
+}
+
+// dst[c * ldd + r] = src[r * lds + c] for r < rows, c < cols: turns a K-major
+// fp32 operand into an MN-major copy (32 x 32 tiles through padded shared
+// memory; every warp reads and writes 128 contiguous bytes).
+__global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ src,
+                                                            int64_t lds, float* __restrict__ dst,
+                                                            int64_t ldd, int rows, int cols) {
+    __shared__ float t[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int tiles_c = (cols + 31) >> 5;
+    const int64_t tiles = (int64_t)((rows + 31) >> 5) * tiles_c;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int r0 = (int)(tile / tiles_c) * 32, c0 = (int)(tile % tiles_c) * 32;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = r0 + ty + 8 * j, c = c0 + tx;
+            if (r < rows && c < cols) t[ty + 8 * j][tx] = src[(int64_t)r * lds + c];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = c0 + ty + 8 * j, r = r0 + tx;
+            if (r < rows && c < cols) dst[(int64_t)c * ldd + r] = t[tx][ty + 8 * j];
+        }
+        __syncthreads();
+    }
 }
 
 bool aligned16(const void* p, int64_t ld) {
@@ -247,7 +352,20 @@ bool aligned16(const void* p, int64_t ld) {
 
 }  // namespace
 
-int launch_sgemm_f32(const Problem& pr, const DeviceInfo&, cudaStream_t stream) {
+int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
+                         int64_t cols, const DeviceInfo& dev, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return kOk;
+    if (rows > 0x7fffffffLL || cols > 0x7fffffffLL) return kUnsupported;
+    const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+    const int64_t cap = (int64_t)dev.sm_count * 8;
+    const int grid = (int)(tiles < cap ? tiles : cap);
+    transpose_f32_kernel<<<grid, 256, 0, stream>>>(src, lds, dst, ldd, (int)rows, (int)cols);
+    if (cudaGetLastError() != cudaSuccess) return kCuda;
+    note_launch();
+    return kOk;
+}
+
+int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, cudaStream_t stream) {
     SgemmParams sp;
     sp.A = static_cast<const float*>(pr.A);
     sp.B = static_cast<const float*>(pr.B);
@@ -266,19 +384,14 @@ int launch_sgemm_f32(const Problem& pr, const DeviceInfo&, cudaStream_t stream) 
     // A/B variant: K-major (4-byte transposing copies), MN-major 16-byte or 4-byte.
     const int av = pr.a_kmajor ? 0 : (aligned16(pr.A, pr.lda) ? 4 : 1);
     const int bv = pr.b_kmajor ? 0 : (aligned16(pr.B, pr.ldb) ? 4 : 1);
-#define SG_CASE(AV, BV, AK, AVEC, BK_, BVEC) \
-    if (av == AV && bv == BV) return launch_variant<AK, AVEC, BK_, BVEC>(sp, stream);
-    SG_CASE(0, 0, true, 1, true, 1)
-    SG_CASE(0, 4, true, 1, false, 4)
-    SG_CASE(0, 1, true, 1, false, 1)
-    SG_CASE(4, 0, false, 4, true, 1)
-    SG_CASE(4, 4, false, 4, false, 4)
-    SG_CASE(4, 1, false, 4, false, 1)
-    SG_CASE(1, 0, false, 1, true, 1)
-    SG_CASE(1, 4, false, 1, false, 4)
-    SG_CASE(1, 1, false, 1, false, 1)
-#undef SG_CASE
-    return kInvalidArg;
+    switch (config) {
+        case 2: return launch_layout<SgCfg<16, 4, false, 2>>(sp, av, bv, dev.device, stream);
+        case 3: return launch_layout<SgCfg<32, 3, true, 2>>(sp, av, bv, dev.device, stream);
+        case 4: return launch_layout<SgCfg<8, 3, true, 2>>(sp, av, bv, dev.device, stream);
+        case 5: return launch_layout<SgCfg<16, 4, true, 1>>(sp, av, bv, dev.device, stream);
+        case 6: return launch_layout<SgCfg<32, 4, true, 1>>(sp, av, bv, dev.device, stream);
+        default: return launch_layout<SgCfg<16, 4, true, 2>>(sp, av, bv, dev.device, stream);
+    }
 }
 
 }  // namespace libgemm

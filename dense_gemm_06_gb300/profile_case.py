@@ -1,0 +1,85 @@
+"""Run one GEMM workload a few times through the C ABI, for profilers.
+
+    python -m dense_gemm_06_gb300.profile_case --case sgemm --n 8192 --am 0 --bm 0 --reps 3
+    python -m dense_gemm_06_gb300.profile_case --case bf16 --n 8192 --reps 3
+    python -m dense_gemm_06_gb300.profile_case --case f16skinny --reps 3
+
+Inputs are the seeded synthetic operands of the benchmark (datagen), resident
+on the device before the first launch; each repetition is one gemm() call on
+one stream, so a profiler sees exactly `reps` launches of the kernel (plus a
+repack launch per misaligned operand for the ragged case). Prints the
+CUDA-event time of every repetition (not a benchmark number).
+"""
+
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+CASES = {
+    # name: (M, N, K, dtype, a_major, b_major, dist, seed, lo, hi)
+    "sgemm": (8192, 8192, 8192, 0, 0, 0, "normal", 1027, 0, 0),
+    "bf16": (8192, 8192, 8192, 4, 0, 0, "normal", 1028, 0, 0),
+    "f16ragged": (4095, 3071, 1037, 1, 0, 1, "int", 1029, -3, 3),
+    "f16skinny": (16384, 256, 8192, 1, 0, 1, "int", 1030, -3, 3),
+}
+
+
+def main(argv=None):
+    import torch
+
+    import datagen
+    import dense_gemm_06_gb300 as lg
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=sorted(CASES), required=True)
+    ap.add_argument("--n", type=int, default=None, help="override M = N = K")
+    ap.add_argument("--am", type=int, default=None)
+    ap.add_argument("--bm", type=int, default=None)
+    ap.add_argument("--cta-group", type=int, default=0)
+    ap.add_argument("--simt-config", type=int, default=0)
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args(argv)
+    M, N, K, dtype, am, bm, dist, seed, lo, hi = CASES[a.case]
+    if a.n:
+        M = N = K = a.n
+    am = am if a.am is None else a.am
+    bm = bm if a.bm is None else a.bm
+    it, ot = lg.IN_TYPE[dtype], lg.OUT_TYPE[dtype]
+    lda = K if am == 0 else M
+    ldb = K if bm == 0 else N
+    A = datagen.operand(M, K, major=am, ld=lda, dtype=it, dist=dist, seed=seed, stream=0,
+                        lo=lo, hi=hi)
+    B = datagen.operand(N, K, major=bm, ld=ldb, dtype=it, dist=dist, seed=seed, stream=1,
+                        lo=lo, hi=hi)
+    torch.cuda.set_device(0)
+    lg.load()
+    conv = (lambda x: x.view(np.int16)) if it != "f32" else (lambda x: x)
+    dA = torch.from_numpy(conv(A)).cuda()
+    dB = torch.from_numpy(conv(B)).cuda()
+    dC = torch.empty(M * N, dtype=torch.float32 if ot == "f32" else torch.int16, device="cuda")
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_CTA_GROUP, a.cta_group))
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, a.simt_config))
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for r in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        lg.check(lg.gemm(M, N, K, dA, lda, am, dB, ldb, bm, dC, N, 1, dtype, s.cuda_stream))
+        e1.record(s)
+        s.synchronize()
+        ms = e0.elapsed_time(e1)
+        print(f"{a.case} {M}x{N}x{K} rep {r}: {ms:.3f} ms, "
+              f"{2.0 * M * N * K / (ms * 1e-3) / 1e12:.1f} TFLOP/s")
+    lg.check(lg.gemm_check_device_error(s.cuda_stream))
+
+
+if __name__ == "__main__":
+    main()

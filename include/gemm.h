@@ -28,7 +28,8 @@
  * For C the enum slot GEMM_MAJOR_K means "M contiguous" (C has no K mode).
  * Any leading dimension and any base address aligned to the element size is
  * accepted (the pages' kernels need 16-byte aligned contiguous dimensions;
- * this library repacks misaligned A/B into 16-byte aligned scratch and stores
+ * this library repacks misaligned 16-bit A/B into 16-byte aligned scratch,
+ * may transpose large K-major fp32 A/B into MN-major scratch, and stores
  * misaligned C with predicated scalar stores).
  *
  * Types (dtype argument):
@@ -167,7 +168,22 @@ enum gemm_option {
        epilogue wait on a barrier that nothing completes, so every call times
        out (after GEMM_OPT_WAIT_LIMIT_NS) and reports GEMM_ERR_TIMEOUT through
        gemm_check_device_error. 0 (default) = off. */
-    GEMM_OPT_TC_FAULT_INJECT = 3
+    GEMM_OPT_TC_FAULT_INJECT = 3,
+    /* Tile configuration of the fp32 FFMA kernel (all 128 x 128 CTA tiles,
+       256 threads, 8 x 8 outputs per thread), as (k-depth, ring stages,
+       FMA form, CTAs per SM the registers are sized for): 0 = automatic,
+       1 = (16, 4, packed, 2), 2 = (16, 4, scalar, 2), 3 = (32, 3, packed, 2),
+       4 = (8, 3, packed, 2) -- the CuTe Ampere example's 128 x 128 x 8 with
+       3 stages --, 5 = (16, 4, packed, 1), 6 = (32, 4, packed, 1). "Packed"
+       is the two-lane fma.rn.f32x2. Every configuration rounds each
+       multiply-add once (IEEE fma) and sums k in the same order. */
+    GEMM_OPT_SIMT_CONFIG = 4,
+    /* K-major fp32 operands: 0 = automatic (an operand is first transposed
+       into an MN-major copy in pool scratch when the other output dimension
+       is >= 512 and M*N*K >= 2^31; the FFMA kernel reads MN-major tiles with
+       16-byte copies), 1 = never transpose (transposing 4-byte copies into
+       shared memory instead), 2 = always transpose. */
+    GEMM_OPT_SIMT_TRANSPOSE = 5
 };
 
 /* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */

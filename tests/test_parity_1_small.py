@@ -137,3 +137,29 @@ def test_empty_m_or_n_is_a_no_op(dtype):
 @pytest.mark.parametrize("dtype", [lg.GEMM_F32, lg.GEMM_F16_F32])
 def test_k_one(dtype):
     run_and_check(129, 257, 1, dtype, 1, 0, 1, dist="int", seed=2)
+
+
+@pytest.mark.parametrize("config", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("am,bm", list(itertools.product((0, 1), (0, 1))))
+def test_sgemm_every_tile_config(config, am, bm):
+    old = lg.gemm_get_option(lg.GEMM_OPT_SIMT_CONFIG)
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, config))
+    try:
+        run_and_check(257, 131, 100, lg.GEMM_F32, am, bm, 1, dist="pm1", seed=config)
+        run_and_check(130, 260, 77, lg.GEMM_F32, am, bm, 0, dist="int", seed=config,
+                      lda_pad=1, ldb_pad=2)
+    finally:
+        lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, old)
+
+
+@pytest.mark.parametrize("transpose", [1, 2])
+@pytest.mark.parametrize("am,bm,cm", list(itertools.product((0, 1), (0, 1), (0, 1))))
+def test_sgemm_with_and_without_operand_transpose(transpose, am, bm, cm):
+    old = lg.gemm_get_option(lg.GEMM_OPT_SIMT_TRANSPOSE)
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_TRANSPOSE, transpose))
+    try:
+        run_and_check(301, 163, 97, lg.GEMM_F32, am, bm, cm, dist="pm1", seed=11,
+                      lda_pad=3, ldb_pad=1, ldc_pad=2)
+        run_and_check(64, 96, 33, lg.GEMM_F32, am, bm, cm, dist="int", seed=12)
+    finally:
+        lg.gemm_set_option(lg.GEMM_OPT_SIMT_TRANSPOSE, old)
