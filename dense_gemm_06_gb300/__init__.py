@@ -36,7 +36,7 @@ IN_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f16", GEMM_BF16_F32: "bf16",
 OUT_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f32", GEMM_BF16_F32: "f32",
             GEMM_F16_F16: "f16", GEMM_BF16_BF16: "bf16"}
 
-EXPORTS = ("gemm", "gemm_host", "gemm_strerror", "gemm_check_device_error",
+EXPORTS = ("gemm", "gemm_host", "gemm_noalloc", "gemm_strerror", "gemm_check_device_error",
            "gemm_release_workspace", "gemm_launch_count", "gemm_set_option",
            "gemm_get_option")
 
@@ -63,7 +63,7 @@ def load(path: str = LIB_PATH):
         lib = ctypes.CDLL(path)
         i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         sig = [i64, i64, i64, vp, i64, ci, vp, i64, ci, vp, i64, ci, ci, vp]
-        for name in ("gemm", "gemm_host"):
+        for name in ("gemm", "gemm_host", "gemm_noalloc"):
             f = getattr(lib, name)
             f.restype, f.argtypes = ci, sig
         lib.gemm_strerror.restype, lib.gemm_strerror.argtypes = ctypes.c_char_p, [ci]
@@ -114,6 +114,14 @@ def gemm_host(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype,
     """The same product on host buffers (copies inside, on `stream`)."""
     return load().gemm_host(M, N, K, _ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C),
                             ldc, c_major, dtype, _stream(stream))
+
+
+def gemm_noalloc(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype,
+                 stream=None) -> int:
+    """The 16-bit product with no device allocation (fixed 32 MiB repack
+    scratch inside the library); see include/gemm.h."""
+    return load().gemm_noalloc(M, N, K, _ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C),
+                               ldc, c_major, dtype, _stream(stream))
 
 
 def gemm_strerror(status: int) -> str:

@@ -291,6 +291,28 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_
 
 void note_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+               const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
+               int dtype) {
+    return validate(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+}
+
+Problem normalised(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+                   const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
+                   int dtype) {
+    return normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+}
+
+int error_word_address(unsigned int** out) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    *out = static_cast<unsigned int*>(p);
+    return kOk;
+}
+
 }  // namespace libgemm
 
 using namespace libgemm;

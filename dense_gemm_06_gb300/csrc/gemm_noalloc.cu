@@ -1,0 +1,190 @@
+// gemm_noalloc.cu -- gemm_noalloc(): the 16-bit tensor-core GEMM for callers
+// that must not allocate device memory.
+//
+// gemm() takes scratch for repacking A or B (rows whose byte pitch or base is
+// not a multiple of 16, which TMA cannot read) from a stream-ordered pool, and
+// the pool may have to grow. Some callers cannot allow that: a serving loop
+// that has reserved all device memory up front for its own allocator, or a
+// latency-critical path where a device allocation (and the synchronisation
+// cudaMalloc may imply) is not acceptable after start-up. For them this entry
+// point repacks into a fixed array that lives in the library's own device
+// image instead, and never calls cudaMalloc, cudaFree or any other
+// allocating routine.
+//
+// The array (kFixedScratchBytes = 32 MiB) is a file-scope __device__ variable,
+// so every GPU that loads the library holds it until the process exits. In
+// host code its name is only a host-side stand-in, never a device address:
+// the address is looked up once per device with cudaGetSymbolAddress (with
+// that device current) and passed to the kernels.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/gemm.h"
+#include "internal.h"
+
+namespace libgemm {
+namespace {
+
+constexpr int64_t kFixedScratchBytes = 32ll << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+
+struct FixedDevice {
+    std::once_flag once;
+    int status = kOk;
+    DeviceInfo info{};
+    unsigned char* scratch = nullptr;  // device address of g_fixed_scratch
+};
+FixedDevice g_fixed[kMaxDevices];
+
+// One-time set-up for the current device (run by its first gemm_noalloc call).
+int fixed_device(FixedDevice** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return kUnsupported;
+    }
+    FixedDevice& st = g_fixed[dev];
+    std::call_once(st.once, [&st, dev] {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            st.status = kUnsupported;
+            return;
+        }
+        if (major != 10 || minor != 3) {
+            st.status = kUnsupported;
+            return;
+        }
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fixed_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            st.status = kCuda;
+            return;
+        }
+        unsigned int* err = nullptr;
+        if (error_word_address(&err) != kOk) {
+            st.status = kCuda;
+            return;
+        }
+        st.scratch = static_cast<unsigned char*>(p);
+        st.info.device = dev;
+        st.info.sm_count = sms;
+        st.info.cc_major = major;
+        st.info.cc_minor = minor;
+        st.info.err_word = err;
+        st.status = kOk;
+    });
+    if (st.status != kOk) return st.status;
+    *out = &st;
+    return kOk;
+}
+
+// Copy `outer` rows of `inner` 16-bit elements (row pitch `lds`) into the
+// fixed array at byte offset `off`, rows `ldd` elements apart.
+__global__ void repack16_fixed_kernel(const uint16_t* __restrict__ src, int64_t lds,
+                                      int64_t off, int64_t ldd, int64_t outer, int64_t inner) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(g_fixed_scratch + off);
+    const int64_t total = outer * inner;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / inner, c = i - r * inner;
+        dst[r * ldd + c] = src[r * lds + c];
+    }
+}
+
+// C = 0 for K == 0: `rows` rows of `row_bytes` bytes, `pitch` bytes apart.
+__global__ void zero_fixed_kernel(unsigned char* C, int64_t rows, int64_t row_bytes,
+                                  int64_t pitch) {
+    const int64_t total = rows * row_bytes;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / row_bytes;
+        C[r * pitch + (i - r * row_bytes)] = 0;
+    }
+}
+
+bool rows_tma_ready(const void* p, int64_t ld) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ((ld * 2) & 15) == 0;
+}
+
+}  // namespace
+}  // namespace libgemm
+
+using namespace libgemm;
+
+extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                            int a_major, const void* B, int64_t ldb, int b_major, void* C,
+                            int64_t ldc, int c_major, int dtype, void* stream) {
+    try {
+        if (dtype == GEMM_F32) return kUnsupported;  // 16-bit inputs only
+        int rc = check_args(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+        if (rc != kOk) return rc;
+        if (M == 0 || N == 0) return kOk;
+        Problem p = normalised(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major,
+                               dtype);
+        if (K == 0) {  // C = 0, as gemm() does
+            FixedDevice* fd = nullptr;
+            rc = fixed_device(&fd);
+            if (rc != kOk) return rc;
+            const int64_t esize = dtype <= GEMM_BF16_F32 ? 4 : 2;
+            int64_t blocks = (p.M * p.N * esize + 255) / 256;
+            const int64_t cap = (int64_t)fd->info.sm_count * 8;
+            if (blocks > cap) blocks = cap;
+            zero_fixed_kernel<<<(int)(blocks < 1 ? 1 : blocks), 256, 0,
+                                static_cast<cudaStream_t>(stream)>>>(
+                static_cast<unsigned char*>(p.C), p.M, p.N * esize, p.ldc * esize);
+            if (cudaGetLastError() != cudaSuccess) return kCuda;
+            note_launch();
+            return kOk;
+        }
+
+        // Plan the repacked copies inside the fixed array before launching
+        // anything, and reject problems that do not fit.
+        const void** ops[2] = {&p.A, &p.B};
+        int64_t* lds[2] = {&p.lda, &p.ldb};
+        const bool kmaj[2] = {p.a_kmajor, p.b_kmajor};
+        const int64_t rows[2] = {p.M, p.N};
+        int64_t off[2] = {-1, -1}, ld2[2] = {0, 0}, inner[2] = {0, 0}, outer[2] = {0, 0};
+        int64_t used = 0;
+        for (int i = 0; i < 2; ++i) {
+            if (rows_tma_ready(*ops[i], *lds[i])) continue;
+            inner[i] = kmaj[i] ? p.K : rows[i];
+            outer[i] = kmaj[i] ? rows[i] : p.K;
+            ld2[i] = (inner[i] + 7) / 8 * 8;
+            const int64_t bytes = (outer[i] * ld2[i] * 2 + 255) / 256 * 256;
+            if (bytes > kFixedScratchBytes - used) return kInvalidArg;  // over the limit
+            off[i] = used;
+            used += bytes;
+        }
+
+        FixedDevice* fd = nullptr;
+        rc = fixed_device(&fd);
+        if (rc != kOk) return rc;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        for (int i = 0; i < 2; ++i) {
+            if (off[i] < 0) continue;
+            int64_t blocks = (outer[i] * inner[i] + 255) / 256;
+            const int64_t cap = (int64_t)fd->info.sm_count * 8;
+            if (blocks > cap) blocks = cap;
+            repack16_fixed_kernel<<<(int)(blocks < 1 ? 1 : blocks), 256, 0, s>>>(
+                static_cast<const uint16_t*>(*ops[i]), *lds[i], off[i], ld2[i], outer[i],
+                inner[i]);
+            if (cudaGetLastError() != cudaSuccess) return kCuda;
+            note_launch();
+            *ops[i] = fd->scratch + off[i];
+            *lds[i] = ld2[i];
+        }
+        int64_t wait = gemm_get_option(GEMM_OPT_WAIT_LIMIT_NS);
+        return launch_gemm_tc(p, fd->info, (int)gemm_get_option(GEMM_OPT_TC_CTA_GROUP),
+                              (uint64_t)(wait > 0 ? wait : 1000000000ll),
+                              (int)gemm_get_option(GEMM_OPT_TC_FAULT_INJECT), s);
+    } catch (...) {
+        return kCuda;
+    }
+}

@@ -42,6 +42,16 @@ int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, int cta_group,
 
 void note_launch(uint64_t n = 1);
 
+// Host-side argument checks and layout normalisation of gemm() (no CUDA calls),
+// and the current device's error-word address (cudaGetSymbolAddress only).
+int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+               const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
+               int dtype);
+Problem normalised(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+                   const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
+                   int dtype);
+int error_word_address(unsigned int** out);
+
 // Status codes shared with the public header (kept numerically identical).
 enum : int {
     kOk = 0,

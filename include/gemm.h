@@ -129,6 +129,38 @@ int gemm_host(int64_t M, int64_t N, int64_t K,
               void *C, int64_t ldc, int c_major,
               int dtype, void *stream);
 
+/*
+ * gemm_noalloc -- the same product for the 16-bit types (GEMM_F16_F32,
+ * GEMM_BF16_F32, GEMM_F16_F16, GEMM_BF16_BF16) without allocating any device
+ * memory. This entry point has no counterpart in the pages; it exists for
+ * callers that cannot allocate: a program whose own allocator has already
+ * reserved the device memory, or a latency-critical loop in which a device
+ * allocation (and the synchronisation it may bring) is not acceptable.
+ *
+ * Where gemm() would repack an operand whose rows are not 16-byte aligned
+ * into pool scratch, gemm_noalloc() repacks it into a fixed 32 MiB array
+ * inside the library's device image, which every GPU that loads the library
+ * holds until the process exits. Limit: the repacked operands together must
+ * fit in 32 MiB (each takes rows x (contiguous extent rounded up to 8
+ * elements) x 2 bytes, rounded up to 256 bytes; operands that are already
+ * aligned take nothing); a larger problem returns GEMM_ERR_INVALID_ARG and
+ * launches nothing. GEMM_F32 returns GEMM_ERR_UNSUPPORTED.
+ *
+ * All calls share the array and it keeps the last call's contents; nothing in
+ * it needs to start at zero (each call rewrites every element its kernel
+ * reads). Calls whose work overlaps on the GPU -- on different streams, or on
+ * different threads without ordering -- race on the array; order them on one
+ * stream. The first call on a device looks the array up on that device
+ * (cudaGetSymbolAddress) and caches the address; make that first call before
+ * any stream capture. Otherwise arguments, layouts, status codes and
+ * asynchrony are those of gemm().
+ */
+int gemm_noalloc(int64_t M, int64_t N, int64_t K,
+                 const void *A, int64_t lda, int a_major,
+                 const void *B, int64_t ldb, int b_major,
+                 void *C, int64_t ldc, int c_major,
+                 int dtype, void *stream);
+
 /* gemm_strerror -- a static, NUL-terminated description of a status code. */
 const char *gemm_strerror(int status);
 
