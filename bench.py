@@ -361,7 +361,7 @@ def profiled_traffic(kernel: str):
 
 # ------------------------------------------------------ CPU baselines --
 
-CPU_ROWS = 32  # rows of each 8192^3 GEMM the oracle computes per sample
+CPU_ROWS = 160  # rows of each 8192^3 GEMM the oracle computes per sample (~10 s)
 
 
 def oracle_sample(f32, bf, rows_per_gemm):

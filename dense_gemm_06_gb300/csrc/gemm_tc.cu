@@ -28,8 +28,9 @@
 //     epilogue warps of both CTAs);
 //   * epilogue: each warp reads its 32 TMEM lanes (= 32 rows of C) in 32-column
 //     chunks with tcgen05.ld, converts (fp32 as is, fp16/bf16 round to nearest
-//     even) and stores straight to global memory, 16-byte vectors where the
-//     row allows and predicated scalars at ragged edges;
+//     even), transposes the chunk through a swizzled shared-memory tile and
+//     stores it row by row -- 16-byte vectors where C's rows allow, coalesced
+//     predicated scalars at ragged edges or misaligned leading dimensions;
 //   * every mbarrier wait is bounded: past `wait_limit_ns` (or once another
 //     wait has failed) the thread records a timeout in the device error word
 //     and its role stops; the CTA drains in-flight copies and MMAs before
@@ -73,7 +74,9 @@ template <int CG> struct Cfg {
     // then the TMEM address slot
     static constexpr int NUM_BARS = 2 * STAGES + 6;
     static constexpr int BAR_BYTES = NUM_BARS * 8 + 8;
-    static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;  // + alignment slack
+    // epilogue staging: one 32 x 128-byte tile per epilogue warp
+    static constexpr int EPI_BYTES = 4 * 32 * 128;
+    static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + align slack
 };
 
 struct TcParams {
@@ -135,51 +138,107 @@ __device__ __noinline__ void grace_period_ns(uint64_t ns) {
     }
 }
 
+// Shared-memory helpers for the epilogue staging tile.
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(a), "r"(x), "r"(y), "r"(z),
+                 "r"(w) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+    return v;
+}
+
+// Position of 16-byte unit u of staging row r: u ^ swz(r). For fp32 a read
+// pass covers one row per quarter-warp and swz(r) = r & 7 suffices; for
+// 16-bit outputs a quarter-warp reads units 0..3 of two consecutive rows, so
+// swz puts rows 2i and 2i+1 in opposite halves. Both are permutations of
+// 0..7 over 8 consecutive rows, which keeps the row-wise writes conflict-free.
+template <int ESIZE>
+__device__ __forceinline__ int swz(int r) {
+    if constexpr (ESIZE == 4) return r & 7;
+    else return ((r & 1) << 2) | ((r >> 1) & 3);
+}
+
+// Writes one 32 x 32 chunk of C: thread `lane` holds row (row0 + lane),
+// columns col0 .. col0+31 in v[]. The chunk goes through the warp's staging
+// tile (32 rows of 128 bytes, units swizzled as above, so both the row-wise
+// writes and the column-wise reads are free of bank conflicts) and leaves it
+// row by row, so every store instruction writes whole row segments of C
+// (16-byte vectors when C's rows are 16-byte aligned, coalesced scalars at
+// ragged edges otherwise).
 template <typename OutT>
-__device__ __forceinline__ void store_chunk(const TcParams& p, int row, int col,
-                                            const uint32_t (&v)[32]) {
-    if (row >= p.M) return;
-    OutT* crow = static_cast<OutT*>(p.C) + (int64_t)row * p.ldc;
+__device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, int lane, int row0,
+                                            int col0, const uint32_t (&v)[32]) {
+    const uint32_t my_row = stage + (uint32_t)lane * 128u;
     if constexpr (sizeof(OutT) == 4) {
-        if (p.c_vec && col + 32 <= p.N) {
-            float4* dst = reinterpret_cast<float4*>(crow + col);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                     __uint_as_float(v[4 * i + 2]),
-                                     __uint_as_float(v[4 * i + 3]));
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (col + i < p.N) crow[col + i] = __uint_as_float(v[i]);
-        }
+        for (int u = 0; u < 8; ++u)
+            sts128(my_row + (uint32_t)((u ^ swz<4>(lane)) * 16), v[4 * u], v[4 * u + 1],
+                   v[4 * u + 2], v[4 * u + 3]);
     } else {
-        uint32_t packed[16];
+        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float lo = __uint_as_float(v[2 * i]), hi = __uint_as_float(v[2 * i + 1]);
             if constexpr (std::is_same<OutT, __nv_bfloat16>::value) {
                 __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
-                packed[i] = *reinterpret_cast<uint32_t*>(&h2);
+                pk[i] = *reinterpret_cast<uint32_t*>(&h2);
             } else {
                 __half2 h2 = __floats2half2_rn(lo, hi);
-                packed[i] = *reinterpret_cast<uint32_t*>(&h2);
+                pk[i] = *reinterpret_cast<uint32_t*>(&h2);
             }
         }
-        if (p.c_vec && col + 32 <= p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + col);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                    packed[4 * i + 3]);
-        } else {
-            uint16_t* c16 = reinterpret_cast<uint16_t*>(crow);
+        for (int u = 0; u < 4; ++u)
+            sts128(my_row + (uint32_t)((u ^ swz<2>(lane)) * 16), pk[4 * u], pk[4 * u + 1],
+                   pk[4 * u + 2], pk[4 * u + 3]);
+    }
+    __syncwarp();
+    constexpr int PER_UNIT = 16 / (int)sizeof(OutT);  // elements per 16-byte unit
+    constexpr int UNITS = 32 / PER_UNIT;               // 16-byte units per row
+    constexpr int ROWS_PER_PASS = 32 / UNITS;
+    if (p.c_vec && col0 + 32 <= p.N) {
+        const int u = lane % UNITS;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (col + i < p.N)
-                    c16[col + i] = (uint16_t)((packed[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu);
+        for (int j = 0; j < 32 / ROWS_PER_PASS; ++j) {
+            const int r = j * ROWS_PER_PASS + lane / UNITS;
+            const uint4 val =
+                lds128(stage + (uint32_t)r * 128u + (uint32_t)((u ^ swz<sizeof(OutT)>(r)) * 16));
+            if (row0 + r < p.M) {
+                OutT* dst = static_cast<OutT*>(p.C) + (int64_t)(row0 + r) * p.ldc + col0 + u * PER_UNIT;
+                *reinterpret_cast<uint4*>(dst) = val;
+            }
+        }
+    } else {
+        const int col = col0 + lane;
+        const int u = lane / PER_UNIT, e = lane % PER_UNIT;
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+            const uint32_t a = stage + (uint32_t)r * 128u +
+                               (uint32_t)((u ^ swz<sizeof(OutT)>(r)) * 16) +
+                               (uint32_t)(e * sizeof(OutT));
+            if (row0 + r < p.M && col < p.N) {
+                OutT* dst = static_cast<OutT*>(p.C) + (int64_t)(row0 + r) * p.ldc + col;
+                if constexpr (sizeof(OutT) == 4)
+                    *reinterpret_cast<uint32_t*>(dst) = lds32(a);
+                else
+                    *reinterpret_cast<uint16_t*>(dst) = lds16(a);
+            }
         }
     }
+    __syncwarp();  // the tile is rewritten by the next chunk
 }
 
 template <int CG, bool A_MN, bool B_MN, bool BF16, typename OutT>
@@ -193,14 +252,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 
     const uint32_t sA0 = base;
     const uint32_t sB0 = base + C_::STAGES * C_::A_BYTES;
-    const uint32_t bar0 = base + C_::RING_BYTES;
+    const uint32_t epi0 = base + C_::RING_BYTES;
+    const uint32_t bar0 = epi0 + C_::EPI_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (C_::STAGES + s); };
     auto accf_bar = [&](int a) { return bar0 + 8u * (2 * C_::STAGES + a); };
     auto acce_bar = [&](int a) { return bar0 + 8u * (2 * C_::STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * C_::STAGES + 4);
     const uint32_t never_bar = bar0 + 8u * (2 * C_::STAGES + 5);  // nothing ever arrives
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::RING_BYTES + 8 * C_::NUM_BARS);
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + C_::RING_BYTES + C_::EPI_BYTES + 8 * C_::NUM_BARS);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -335,14 +396,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 break;
             }
             tc_fence_after_sync();
-            const int row = tc.tm * C_::TILE_M + (int)rank * ROWS_A + q * 32 + lane;
+            const int row0 = tc.tm * C_::TILE_M + (int)rank * ROWS_A + q * 32;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+            const uint32_t stage = epi0 + (uint32_t)(q * 32 * 128);
 #pragma unroll 1
             for (int c = 0; c < ACC_COLS / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
                 tmem_wait_ld();
-                store_chunk<OutT>(p, row, tc.tn * TILE_N + c * 32, v);
+                store_chunk<OutT>(p, stage, lane, row0, tc.tn * TILE_N + c * 32, v);
             }
             tc_fence_before_sync();
             __syncwarp();
