@@ -116,25 +116,41 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.out.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 7:
-                    continue
-                try:
-                    rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
-                except ValueError:
-                    continue
+            lines = f.readlines()
         os.remove(self.path)
-        if not rows:
-            return None
-        sm = [r[0] for r in rows]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v == "Active"})
-        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        return summarize_clocks(lines)
+
+
+CLOCK_REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def summarize_clocks(lines):
+    """Median SM clock under load, max clock and the throttle reasons seen,
+    from nvidia-smi CSV rows (ClockSampler.FIELDS, no header, no units)."""
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 7:
+            continue
+        try:
+            rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    sm = [r[0] for r in rows]
+    reasons = sorted({CLOCK_REASONS[i] for r in rows for i, v in enumerate(r[2])
+                      if v == "Active"})
+    loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": reasons, "samples": len(rows)}
+
+
+def throughput_tflops(flops_per_step, steps, world, ms):
+    """Whole-job TFLOP/s: every rank ran `steps` steps; `ms` is the slowest
+    rank's device time (weak scaling over replicas)."""
+    return flops_per_step * steps * world / (ms * 1e-3) / 1e12
 
 
 # ------------------------------------------------------- native arm --
@@ -218,7 +234,7 @@ def run_native(args):
         return
     peaks, peak_src = load_peaks()
     flops_step = FLOPS_PER_GEMM * n_gemms
-    value = flops_step * args.steps * world / (ms_total * 1e-3) / 1e12
+    value = throughput_tflops(flops_step, args.steps, world, ms_total)
     parts = []
     for i, (name, am, bm) in enumerate(GEMMS):
         tf = FLOPS_PER_GEMM / (per_ms[i] * 1e-3) / 1e12
@@ -266,6 +282,7 @@ def barrier(world):
 
 
 def max_over_ranks(x, world, dev):
+    """The largest `x` over all ranks (the job's time is the slowest rank's)."""
     if world == 1:
         return x
     import torch
@@ -308,7 +325,7 @@ def run_e2e(args, lg, f32, bf, stream, world, dev):
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     h2d = 4 * 2 * n * n * 4 + 2 * n * n * 2
     d2h = 4 * n * n * 4 + n * n * 2
-    return {"value": round(FLOPS_PER_GEMM * 5 * steps * world / (ms * 1e-3) / 1e12, 3),
+    return {"value": round(throughput_tflops(FLOPS_PER_GEMM * 5, steps, world, ms), 3),
             "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(ms / steps, 3),
             "api": "gemm_host (C ABI, pinned host buffers)"}
@@ -361,7 +378,7 @@ def profiled_traffic(kernel: str):
 
 # ------------------------------------------------------ CPU baselines --
 
-CPU_ROWS = 160  # rows of each 8192^3 GEMM the oracle computes per sample (~10 s)
+CPU_ROWS = 400  # rows of each 8192^3 GEMM the oracle computes per sample (~10 s)
 
 
 def oracle_sample(f32, bf, rows_per_gemm):

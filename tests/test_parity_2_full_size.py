@@ -1,24 +1,25 @@
-"""GPU parity on the five benchmark workloads at their full sizes, in the launch
-configuration the benchmark times (default options: the 2-CTA tensor-core
-kernel, the FFMA kernel for fp32).
+"""GPU parity on the full-size workloads, in the launch configuration the
+benchmark times (default options: the 2-CTA tensor-core kernel, the FFMA
+kernel for fp32).
 
-1. 1024 x 512 x 256 fp16 integers in [-5, 5] (A, B K-major) -> fp32 C
+* 1024 x 512 x 256 fp16 integers in [-5, 5] (A, B K-major) -> fp32 C
    row-major: the CK Tile practice GEMM's "Problem Size Configuration" and
    integer fill; bit-exact against the full oracle.
-2. 2048^3 fp32 SGEMM, A M-major, B N-major, C N-major, U[-1, 1]: the CuTe
+* 2048^3 fp32 SGEMM, A M-major, B N-major, C N-major, U[-1, 1]: the CuTe
    Ampere SGEMM example's documented layout (a_major m, b_major n, c_major
    n); full oracle, |C - C_ref| <= 1e-4 * S.
-3. 8192^3 fp32 SGEMM over all four A/B majors, N(0, 1): the CuTe example's
+* 8192^3 fp32 SGEMM over all four A/B majors, N(0, 1): the CuTe example's
    ncu recipe size; 256 seeded rows and 256 seeded columns (plus the first
    and last) against the oracle.
-4. 8192^3 bf16 -> bf16 (A, B K-major), N(0, 1) rounded to bf16: the Gluon
+* 8192^3 bf16 -> bf16 (A, B K-major), N(0, 1) rounded to bf16: the Gluon
    Multi-CTA tutorial's benchmark size; sampled rows/columns, 1 bf16 ulp +
    1e-4 * S.
-5. 4095 x 3071 x 1037 (A K-major, B N-major, packed: lda 1037, ldb 3071,
+* 4095 x 3071 x 1037 (A K-major, B N-major, packed: lda 1037, ldb 3071,
    ldc 3071, none 16-byte multiples) and 16384 x 256 x 8192, fp16 integers
    in [-3, 3] -> fp32; bit-exact against the full oracle.
 
-Seeds are 1024 + workload number (5a: 1029, 5b: 1030).
+Seeds: 1025 (1024 x 512 x 256), 1026 (2048^3), 1027 (8192^3 fp32), 1028
+(8192^3 bf16), 1029 (4095 x 3071 x 1037), 1030 (16384 x 256 x 8192).
 """
 
 import numpy as np
@@ -40,23 +41,23 @@ def _lib():
 
 
 @pytest.mark.parametrize("cta_group", [0, 1])
-def test_config1_1024x512x256_fp16_int(cta_group):
+def test_fp16_int_1024x512x256_bit_exact(cta_group):
     M, N, K = 1024, 512, 256
     A, lda, B, ldb = make_operands(M, N, K, lg.GEMM_F16_F32, 0, 0, "int", 1025)
     C = run_device_gemm(M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 0, cta_group=cta_group)
     check_full(C, M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 0, exact=True,
-               what=f"config 1 (cg={cta_group})")
+               what=f"1024x512x256 fp16 int (cg={cta_group})")
 
 
-def test_config2_2048_fp32():
+def test_fp32_2048_cubed_a_m_b_n():
     M = N = K = 2048
     A, lda, B, ldb = make_operands(M, N, K, lg.GEMM_F32, 1, 1, "pm1", 1026)
     C = run_device_gemm(M, N, K, lg.GEMM_F32, A, lda, 1, B, ldb, 1)
-    check_full(C, M, N, K, lg.GEMM_F32, A, lda, 1, B, ldb, 1, exact=False, what="config 2")
+    check_full(C, M, N, K, lg.GEMM_F32, A, lda, 1, B, ldb, 1, exact=False, what="2048^3 fp32")
 
 
 @pytest.fixture(scope="module")
-def cfg3_logical():
+def fp32_8192_logical():
     n = 8192
     LA = datagen.logical(n, n, dtype="f32", dist="normal", seed=1027, stream=0)
     LB = datagen.logical(n, n, dtype="f32", dist="normal", seed=1027, stream=1)
@@ -64,35 +65,35 @@ def cfg3_logical():
 
 
 @pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
-def test_config3_8192_fp32_all_majors(cfg3_logical, am, bm):
+def test_fp32_8192_cubed_all_majors(fp32_8192_logical, am, bm):
     n = 8192
-    LA, LB = cfg3_logical
+    LA, LB = fp32_8192_logical
     A = (LA if am == 0 else LA.T).copy().ravel()
     B = (LB if bm == 0 else LB.T).copy().ravel()
     C = run_device_gemm(n, n, n, lg.GEMM_F32, A, n, am, B, n, bm)
     check_sampled(C, n, n, n, lg.GEMM_F32, A, n, am, B, n, bm, exact=False,
-                  what=f"config 3 A{'KM'[am]} B{'KN'[bm]}", seed=1027)
+                  what=f"8192^3 fp32 A{'KM'[am]} B{'KN'[bm]}", seed=1027)
 
 
 @pytest.mark.parametrize("cta_group", [0, 1])
-def test_config4_8192_bf16(cta_group):
+def test_bf16_8192_cubed(cta_group):
     n = 8192
     A, lda, B, ldb = make_operands(n, n, n, lg.GEMM_BF16_BF16, 0, 0, "normal", 1028)
     C = run_device_gemm(n, n, n, lg.GEMM_BF16_BF16, A, lda, 0, B, ldb, 0, cta_group=cta_group)
     check_sampled(C, n, n, n, lg.GEMM_BF16_BF16, A, lda, 0, B, ldb, 0, exact=False,
-                  what=f"config 4 (cg={cta_group})", seed=1028)
+                  what=f"8192^3 bf16 (cg={cta_group})", seed=1028)
 
 
-def test_config5a_ragged_fp16_int():
+def test_fp16_int_4095x3071x1037_ragged_bit_exact():
     M, N, K = 4095, 3071, 1037
     A, lda, B, ldb = make_operands(M, N, K, lg.GEMM_F16_F32, 0, 1, "int", 1029, lo=-3, hi=3)
     assert (lda, ldb) == (1037, 3071)
     C = run_device_gemm(M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1)
-    check_full(C, M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, exact=True, what="config 5a")
+    check_full(C, M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, exact=True, what="4095x3071x1037 fp16 int")
 
 
-def test_config5b_tall_skinny_fp16_int():
+def test_fp16_int_16384x256x8192_skinny_bit_exact():
     M, N, K = 16384, 256, 8192
     A, lda, B, ldb = make_operands(M, N, K, lg.GEMM_F16_F32, 0, 1, "int", 1030, lo=-3, hi=3)
     C = run_device_gemm(M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1)
-    check_full(C, M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, exact=True, what="config 5b")
+    check_full(C, M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, exact=True, what="16384x256x8192 fp16 int")
