@@ -1,0 +1,52 @@
+"""Failure detection on the GPU without a fault: the tensor-core kernel's
+pipeline waits are time-bounded. With the test hook GEMM_OPT_TC_FAULT_INJECT
+the epilogue waits on a barrier that nothing completes; the wait must run
+out after GEMM_OPT_WAIT_LIMIT_NS, the kernel must wind down (the MMA and
+producer roles see the error word and stop, in-flight work drains, TMEM is
+released), gemm_check_device_error must report GEMM_ERR_TIMEOUT once, and the
+device must stay usable for correct GEMMs afterwards."""
+
+import pytest
+
+import dense_gemm_06_gb300 as lg
+from gpu_util import check_full, make_operands, run_device_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    lg.load()
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_stalled_wait_times_out_and_device_recovers(cta_group):
+    import torch
+    n, k = 4096, 512  # >= 3 tiles per CTA pair: the MMA role also blocks
+    dA = torch.zeros(n * k, dtype=torch.int16, device="cuda")
+    dB = torch.zeros(n * k, dtype=torch.int16, device="cuda")
+    dC = torch.zeros(n * n, dtype=torch.int16, device="cuda")
+    assert lg.gemm_check_device_error() == lg.GEMM_OK
+    saved = {o: lg.gemm_get_option(o) for o in (lg.GEMM_OPT_WAIT_LIMIT_NS,
+                                                lg.GEMM_OPT_TC_FAULT_INJECT,
+                                                lg.GEMM_OPT_TC_CTA_GROUP)}
+    try:
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_WAIT_LIMIT_NS, 20_000_000))
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_CTA_GROUP, cta_group))
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_FAULT_INJECT, 1))
+        rc = lg.gemm(n, n, k, dA, k, 0, dB, k, 0, dC, n, 1, lg.GEMM_BF16_BF16)
+        assert rc == lg.GEMM_OK  # asynchronous: the timeout is reported later
+        assert lg.gemm_check_device_error() == lg.GEMM_ERR_TIMEOUT
+        assert lg.gemm_check_device_error() == lg.GEMM_OK  # the word was cleared
+    finally:
+        for o, v in saved.items():
+            lg.gemm_set_option(o, v)
+    # the context is intact: a normal GEMM on both paths is still exact
+    for dtype in (lg.GEMM_F16_F32, lg.GEMM_F32):
+        A, lda, B, ldb = make_operands(300, 520, 200, dtype, 0, 1, "int", 3)
+        C = run_device_gemm(300, 520, 200, dtype, A, lda, 0, B, ldb, 1, cta_group=cta_group)
+        check_full(C, 300, 520, 200, dtype, A, lda, 0, B, ldb, 1, exact=True,
+                   what=f"after timeout (cg={cta_group})")
