@@ -82,6 +82,8 @@ template <int CG> struct Cfg {
 struct TcParams {
     CUtensorMap tmap_a;
     CUtensorMap tmap_b;
+    CUtensorMap tmap_c;        // valid when c_tma
+    int c_tma;                 // C stored with TMA (16-byte aligned base and rows)
     void* C;
     int64_t ldc;
     int M, N, K;
@@ -160,29 +162,37 @@ __device__ __forceinline__ uint16_t lds16(uint32_t a) {
     return v;
 }
 
-// Position of 16-byte unit u of staging row r: u ^ swz(r). For fp32 a read
-// pass covers one row per quarter-warp and swz(r) = r & 7 suffices; for
-// 16-bit outputs a quarter-warp reads units 0..3 of two consecutive rows, so
-// swz puts rows 2i and 2i+1 in opposite halves. Both are permutations of
-// 0..7 over 8 consecutive rows, which keeps the row-wise writes conflict-free.
+// Epilogue staging tile of one warp: 32 rows of 32 elements, ROW_BYTES =
+// 32 * sizeof(OutT) bytes each; 16-byte unit u of row r sits at unit
+// u ^ swz(r). swz is the TMA swizzle pattern of the row width -- 128-byte
+// swizzle (r & 7) for fp32 rows, 64-byte swizzle ((r >> 1) & 3) for 16-bit
+// rows -- so the tile can be TMA-stored as is, and with it the row-wise
+// writes (a quarter-warp = 8 rows, one unit each) and the column-wise reads
+// of the st.global path are free of bank conflicts.
 template <int ESIZE>
 __device__ __forceinline__ int swz(int r) {
     if constexpr (ESIZE == 4) return r & 7;
-    else return ((r & 1) << 2) | ((r >> 1) & 3);
+    else return (r >> 1) & 3;
 }
 
 // Writes one 32 x 32 chunk of C: thread `lane` holds row (row0 + lane),
 // columns col0 .. col0+31 in v[]. The chunk goes through the warp's staging
-// tile (32 rows of 128 bytes, units swizzled as above, so both the row-wise
-// writes and the column-wise reads are free of bank conflicts) and leaves it
-// row by row, so every store instruction writes whole row segments of C
-// (16-byte vectors when C's rows are 16-byte aligned, coalesced scalars at
-// ragged edges otherwise).
+// tile and leaves it either by one TMA store (C rows 16-byte aligned and the
+// chunk entirely inside C) or row by row with st.global (16-byte vectors when
+// C's rows allow, coalesced predicated scalars otherwise), so every store
+// writes whole row segments of C.
 template <typename OutT>
 __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, int lane, int row0,
                                             int col0, const uint32_t (&v)[32]) {
-    const uint32_t my_row = stage + (uint32_t)lane * 128u;
-    if constexpr (sizeof(OutT) == 4) {
+    constexpr int ES = (int)sizeof(OutT);
+    constexpr int ROW_BYTES = 32 * ES;
+    if (p.c_tma) {
+        // the previous chunk's TMA store must have finished reading the tile
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+    }
+    const uint32_t my_row = stage + (uint32_t)(lane * ROW_BYTES);
+    if constexpr (ES == 4) {
 #pragma unroll
         for (int u = 0; u < 8; ++u)
             sts128(my_row + (uint32_t)((u ^ swz<4>(lane)) * 16), v[4 * u], v[4 * u + 1],
@@ -205,9 +215,20 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
             sts128(my_row + (uint32_t)((u ^ swz<2>(lane)) * 16), pk[4 * u], pk[4 * u + 1],
                    pk[4 * u + 2], pk[4 * u + 3]);
     }
+    // TMA only for chunks entirely inside C; edge chunks take the st.global
+    // path below, so no store ever relies on clipping at the edges of C.
+    if (p.c_tma && row0 + 32 <= p.M && col0 + 32 <= p.N) {
+        fence_proxy_async_smem();  // make the tile visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(&p.tmap_c, stage, col0, row0);
+            bulk_commit_group();
+        }
+        return;
+    }
     __syncwarp();
-    constexpr int PER_UNIT = 16 / (int)sizeof(OutT);  // elements per 16-byte unit
-    constexpr int UNITS = 32 / PER_UNIT;               // 16-byte units per row
+    constexpr int PER_UNIT = 16 / ES;           // elements per 16-byte unit
+    constexpr int UNITS = 32 / PER_UNIT;        // 16-byte units per row
     constexpr int ROWS_PER_PASS = 32 / UNITS;
     if (p.c_vec && col0 + 32 <= p.N) {
         const int u = lane % UNITS;
@@ -215,7 +236,7 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
         for (int j = 0; j < 32 / ROWS_PER_PASS; ++j) {
             const int r = j * ROWS_PER_PASS + lane / UNITS;
             const uint4 val =
-                lds128(stage + (uint32_t)r * 128u + (uint32_t)((u ^ swz<sizeof(OutT)>(r)) * 16));
+                lds128(stage + (uint32_t)(r * ROW_BYTES) + (uint32_t)((u ^ swz<ES>(r)) * 16));
             if (row0 + r < p.M) {
                 OutT* dst = static_cast<OutT*>(p.C) + (int64_t)(row0 + r) * p.ldc + col0 + u * PER_UNIT;
                 *reinterpret_cast<uint4*>(dst) = val;
@@ -226,12 +247,11 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
         const int u = lane / PER_UNIT, e = lane % PER_UNIT;
 #pragma unroll 4
         for (int r = 0; r < 32; ++r) {
-            const uint32_t a = stage + (uint32_t)r * 128u +
-                               (uint32_t)((u ^ swz<sizeof(OutT)>(r)) * 16) +
-                               (uint32_t)(e * sizeof(OutT));
+            const uint32_t a = stage + (uint32_t)(r * ROW_BYTES) +
+                               (uint32_t)((u ^ swz<ES>(r)) * 16) + (uint32_t)(e * ES);
             if (row0 + r < p.M && col < p.N) {
                 OutT* dst = static_cast<OutT*>(p.C) + (int64_t)(row0 + r) * p.ldc + col;
-                if constexpr (sizeof(OutT) == 4)
+                if constexpr (ES == 4)
                     *reinterpret_cast<uint32_t*>(dst) = lds32(a);
                 else
                     *reinterpret_cast<uint16_t*>(dst) = lds16(a);
@@ -414,6 +434,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        if (p.c_tma && lane == 0) bulk_wait_all();  // stores done before the CTA exits
+        __syncwarp();
     }
 
     // ------------------------------------------------------------ teardown --
@@ -548,7 +570,8 @@ int dispatch_types(TcParams& tp, int dtype, bool a_mn, bool b_mn, const DeviceIn
 }  // namespace
 
 int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
-                   uint64_t wait_limit_ns, int fault_inject, cudaStream_t stream) {
+                   uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled,
+                   cudaStream_t stream) {
     if (!get_encoder()) return kCuda;
     const int CG = cta_group == 1 ? 1 : 2;
     const bool bf16 = pr.dtype == 2 || pr.dtype == 4;
@@ -567,6 +590,25 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     if (!ok) return kCuda;
 
     const int out_bytes = pr.dtype <= 2 ? 4 : 2;
+    // C through TMA when its base and rows are 16-byte aligned: box 32 x 32,
+    // the staging tile's swizzle (128-byte rows for fp32, 64-byte for 16-bit).
+    tp.c_tma = 0;
+    if ((reinterpret_cast<uintptr_t>(pr.C) & 15u) == 0 && ((pr.ldc * out_bytes) & 15) == 0 &&
+        c_tma_enabled) {
+        const cuuint64_t dims[2] = {(cuuint64_t)pr.N, (cuuint64_t)pr.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)(pr.ldc * out_bytes)};
+        const cuuint32_t box[2] = {32, 32};
+        const cuuint32_t estr[2] = {1, 1};
+        const CUtensorMapDataType dt = out_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : (bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+        if (g_encode(&tp.tmap_c, dt, 2, pr.C, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+            tp.c_tma = 1;
+    }
     tp.C = pr.C;
     tp.ldc = pr.ldc;
     tp.M = (int)pr.M;

@@ -37,8 +37,11 @@ int launch_sgemm_f32(const Problem& p, const DeviceInfo& dev, int config, cudaSt
 // dst[c * ldd + r] = src[r * lds + c] (fp32), rows x cols.
 int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
                          int64_t cols, const DeviceInfo& dev, cudaStream_t stream);
+// c_tma_enabled: 1 = store C with TMA when its rows are 16-byte aligned,
+// 0 = always use the st.global epilogue.
 int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, int cta_group,
-                   uint64_t wait_limit_ns, int fault_inject, cudaStream_t stream);
+                   uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled,
+                   cudaStream_t stream);
 
 void note_launch(uint64_t n = 1);
 

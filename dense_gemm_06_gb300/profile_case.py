@@ -45,6 +45,7 @@ def main(argv=None):
     ap.add_argument("--bm", type=int, default=None)
     ap.add_argument("--cta-group", type=int, default=0)
     ap.add_argument("--simt-config", type=int, default=0)
+    ap.add_argument("--tc-store", type=int, default=0)
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args(argv)
     M, N, K, dtype, am, bm, dist, seed, lo, hi = CASES[a.case]
@@ -67,6 +68,7 @@ def main(argv=None):
     dC = torch.empty(M * N, dtype=torch.float32 if ot == "f32" else torch.int16, device="cuda")
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_CTA_GROUP, a.cta_group))
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, a.simt_config))
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_STORE, a.tc_store))
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
     for r in range(a.reps):

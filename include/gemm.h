@@ -215,7 +215,12 @@ enum gemm_option {
        is >= 512 and M*N*K >= 2^31; the FFMA kernel reads MN-major tiles with
        16-byte copies), 1 = never transpose (transposing 4-byte copies into
        shared memory instead), 2 = always transpose. */
-    GEMM_OPT_SIMT_TRANSPOSE = 5
+    GEMM_OPT_SIMT_TRANSPOSE = 5,
+    /* How the tensor-core kernel writes C: 0 = automatic (a TMA tensor store
+       of each 32 x 32 chunk that lies entirely inside C when C's base and
+       row pitch are 16-byte aligned; row-coalesced st.global for the other
+       chunks), 1 = always st.global. */
+    GEMM_OPT_TC_STORE = 6
 };
 
 /* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */

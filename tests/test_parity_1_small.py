@@ -38,10 +38,12 @@ def rne16(x: np.ndarray, t: str) -> np.ndarray:
 
 
 def run_and_check(M, N, K, dtype, am, bm, cm=1, dist="int", seed=0, lda_pad=0, ldb_pad=0,
-                  ldc_pad=0, cta_group=0):
+                  ldc_pad=0, cta_group=0, tc_store=0):
     A, lda, B, ldb = make_operands(M, N, K, dtype, am, bm, dist, seed, lda_pad, ldb_pad)
-    C = run_device_gemm(M, N, K, dtype, A, lda, am, B, ldb, bm, cm, ldc_pad, cta_group)
-    what = f"{M}x{N}x{K} dtype={dtype} A{'KM'[am]} B{'KN'[bm]} C{'MN'[cm]} cg={cta_group}"
+    C = run_device_gemm(M, N, K, dtype, A, lda, am, B, ldb, bm, cm, ldc_pad, cta_group,
+                        tc_store=tc_store)
+    what = (f"{M}x{N}x{K} dtype={dtype} A{'KM'[am]} B{'KN'[bm]} C{'MN'[cm]} cg={cta_group} "
+            f"store={tc_store}")
     ot = lg.OUT_TYPE[dtype]
     if dist == "int" and ot != "f32":
         import oracle
@@ -80,20 +82,25 @@ def test_sgemm_padded_and_unaligned_ld(am, bm):
 TC_SHAPES = [(1, 1, 1), (100, 70, 64), (300, 520, 200), (257, 513, 1037)]
 
 
+@pytest.mark.parametrize("tc_store", [0, 1])
 @pytest.mark.parametrize("cta_group", [1, 2])
 @pytest.mark.parametrize("dtype", TC_TYPES)
 @pytest.mark.parametrize("am,bm", list(itertools.product((0, 1), (0, 1))))
 @pytest.mark.parametrize("shape", TC_SHAPES)
-def test_tc_ragged_integer(shape, am, bm, dtype, cta_group):
+def test_tc_ragged_integer(shape, am, bm, dtype, cta_group, tc_store):
+    # tc_store 0: TMA store of C where its rows are 16-byte aligned; 1: st.global
     M, N, K = shape
-    run_and_check(M, N, K, dtype, am, bm, 1, dist="int", seed=K, cta_group=cta_group)
+    run_and_check(M, N, K, dtype, am, bm, 1, dist="int", seed=K, cta_group=cta_group,
+                  tc_store=tc_store)
 
 
+@pytest.mark.parametrize("tc_store", [0, 1])
 @pytest.mark.parametrize("cta_group", [1, 2])
 @pytest.mark.parametrize("dtype", TC_TYPES)
 @pytest.mark.parametrize("cm", [0, 1])
-def test_tc_normal_values(dtype, cm, cta_group):
-    run_and_check(384, 520, 640, dtype, 0, 1, cm, dist="normal", seed=5, cta_group=cta_group)
+def test_tc_normal_values(dtype, cm, cta_group, tc_store):
+    run_and_check(384, 520, 640, dtype, 0, 1, cm, dist="normal", seed=5, cta_group=cta_group,
+                  tc_store=tc_store)
 
 
 @pytest.mark.parametrize("cta_group", [1, 2])
