@@ -33,6 +33,7 @@ std::atomic<int> g_fault_inject{0};
 std::atomic<int> g_simt_config{0};
 std::atomic<int> g_simt_transpose{0};
 std::atomic<int> g_tc_store{0};
+std::atomic<int> g_tc_multicast{0};
 
 struct DeviceState {
     std::once_flag once;
@@ -282,7 +283,8 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_
     }
     if (rc == kOk)
         rc = launch_gemm_tc(p, dev, g_cta_group.load(), g_wait_limit_ns.load(),
-                            g_fault_inject.load(), g_tc_store.load() != 1, s);
+                            g_fault_inject.load(), g_tc_store.load() != 1,
+                            g_tc_multicast.load() == 2, s);
     for (int i = 0; i < 2; ++i)
         if (scratch[i]) cudaFreeAsync(scratch[i], s);
     return rc;
@@ -480,6 +482,10 @@ int gemm_set_option(int option, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             g_tc_store.store((int)value);
             return GEMM_OK;
+        case GEMM_OPT_TC_MULTICAST:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_tc_multicast.store((int)value);
+            return GEMM_OK;
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -492,6 +498,7 @@ int64_t gemm_get_option(int option) {
         case GEMM_OPT_SIMT_CONFIG: return g_simt_config.load();
         case GEMM_OPT_SIMT_TRANSPOSE: return g_simt_transpose.load();
         case GEMM_OPT_TC_STORE: return g_tc_store.load();
+        case GEMM_OPT_TC_MULTICAST: return g_tc_multicast.load();
         default: return -1;
     }
 }

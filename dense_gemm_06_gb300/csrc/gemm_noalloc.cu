@@ -184,7 +184,8 @@ extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int6
         return launch_gemm_tc(p, fd->info, (int)gemm_get_option(GEMM_OPT_TC_CTA_GROUP),
                               (uint64_t)(wait > 0 ? wait : 1000000000ll),
                               (int)gemm_get_option(GEMM_OPT_TC_FAULT_INJECT),
-                              gemm_get_option(GEMM_OPT_TC_STORE) != 1, s);
+                              gemm_get_option(GEMM_OPT_TC_STORE) != 1,
+                              gemm_get_option(GEMM_OPT_TC_MULTICAST) == 2, s);
     } catch (...) {
         return kCuda;
     }

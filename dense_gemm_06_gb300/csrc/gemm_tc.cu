@@ -261,9 +261,13 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
     __syncwarp();  // the tile is rewritten by the next chunk
 }
 
-template <int CG, bool A_MN, bool B_MN, bool BF16, typename OutT>
+template <int CG, bool MC, bool A_MN, bool B_MN, bool BF16, typename OutT>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
     using C_ = Cfg<CG>;
+    // MC: a cluster holds two CTA pairs computing vertically adjacent tiles
+    // that share their B columns; the rank-h CTA of each pair loads half of
+    // B-half h and multicasts it to the rank-h CTAs of both pairs.
+    static_assert(!MC || CG == 2, "operand multicast runs on CTA pairs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 128-byte swizzle atoms must sit on 1024-byte boundaries.
     const uint32_t raw = smem_u32(smem_raw);
@@ -285,18 +289,28 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+    const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;  // rank in the cluster
+    const uint32_t rank = crank & (uint32_t)(CG - 1);          // rank in the CTA pair
+    const int pair = MC ? (int)(crank >> 1) : 0;               // pair in the cluster
+    const uint32_t lead = crank & ~(uint32_t)(CG - 1);         // cluster rank of the pair leader
     const bool leader = rank == 0;
     const int cluster = CG == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
     const int nclusters = CG == 2 ? (int)num_clusters_x() : (int)gridDim.x;
-    const int total_tiles = p.tiles_m * p.tiles_n;
+    // work units: tiles, or (MC) pairs of vertically adjacent tiles
+    const int unit_rows = MC ? (p.tiles_m + 1) / 2 : p.tiles_m;
+    const int total_tiles = unit_rows * p.tiles_n;
+    auto tile_of = [&](int t) {
+        TileCoord tc = raster(t, unit_rows, p.tiles_n);
+        if (MC) tc.tm = tc.tm * 2 + pair;  // may be past the last tile row: all rows OOB
+        return tc;
+    };
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&p.tmap_a);
         tma_prefetch_desc(&p.tmap_b);
         for (int s = 0; s < C_::STAGES; ++s) {
             mbar_init(full_bar(s), 1);   // leader's producer arms it for both CTAs
-            mbar_init(empty_bar(s), 1);  // one (multicast) MMA commit
+            mbar_init(empty_bar(s), MC ? 2 : 1);  // MMA commits of every pair using the stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
@@ -323,12 +337,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
-                const TileCoord tc = raster(t, p.tiles_m, p.tiles_n);
+                const TileCoord tc = tile_of(t);
                 const int a_row = tc.tm * C_::TILE_M + (int)rank * ROWS_A;
                 const int b_row = tc.tn * TILE_N + (int)rank * C_::B_ROWS;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(empty_bar(stage), phase ^ 1u, p)) { aborted = true; break; }
-                    const uint32_t fb = CG == 2 ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+                    const uint32_t fb =
+                        CG == 2 ? mapa_shared(full_bar(stage), lead) : full_bar(stage);
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), CG * C_::STAGE_BYTES);
                     const uint32_t sa = sA0 + stage * C_::A_BYTES;
                     const uint32_t sb = sB0 + stage * C_::B_BYTES;
@@ -340,7 +355,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                         for (int j = 0; j < ROWS_A / 64; ++j)
                             tma_load_2d<CG>(sa + j * 64 * BK * 2, &p.tmap_a, fb, a_row + 64 * j, k0);
                     }
-                    if constexpr (!B_MN) {
+                    if constexpr (MC) {
+                        // this pair's 64-row piece of B-half `rank`, to both pairs
+                        const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+                        const uint32_t dst = sb + (uint32_t)(pair * 64 * BK * 2);
+                        if constexpr (!B_MN)
+                            tma_load_2d_mc_pair(dst, &p.tmap_b, fb, k0, b_row + 64 * pair, mask);
+                        else
+                            tma_load_2d_mc_pair(dst, &p.tmap_b, fb, b_row + 64 * pair, k0, mask);
+                    } else if constexpr (!B_MN) {
                         tma_load_2d<CG>(sb, &p.tmap_b, fb, k0, b_row);
                     } else {
 #pragma unroll
@@ -383,15 +406,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                             : make_sdesc_sw128(sb + j * UMMA_K * 2, 16, 1024);
                         mma_f16<CG>(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                     }
-                    mma_commit<CG>(empty_bar(stage));
+                    if constexpr (MC) mma_commit_pair(empty_bar(stage), (uint16_t)0xF);
+                    else mma_commit<CG>(empty_bar(stage));
                     if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (aborted) break;
-                mma_commit<CG>(accf_bar(acc));
+                if constexpr (MC) mma_commit_pair(accf_bar(acc), (uint16_t)(0x3u << (2 * pair)));
+                else mma_commit<CG>(accf_bar(acc));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             // Drain: wait (bounded) until every MMA issued above has completed.
-            if constexpr (CG == 2) mma_commit_pair(drain_bar, (uint16_t)0x1);
+            if constexpr (CG == 2) mma_commit_pair(drain_bar, (uint16_t)(1u << crank));
             else mma_commit_local(drain_bar);
             uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < 1000000000ull) {
@@ -410,7 +435,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             if (!__all_sync(0xffffffffu, wait_bar(never_bar, 0u, p))) aborted = true;
         }
         for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
-            const TileCoord tc = raster(t, p.tiles_m, p.tiles_n);
+            const TileCoord tc = tile_of(t);
             if (!__all_sync(0xffffffffu, wait_bar(accf_bar(acc), acc_phase, p))) {
                 aborted = true;
                 break;
@@ -429,7 +454,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
-                if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+                if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(acce_bar(acc), lead));
                 else mbar_arrive_local(acce_bar(acc));
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
@@ -487,13 +512,25 @@ bool encode_2d(CUtensorMap* map, bool bf16, const void* ptr, uint64_t inner, uin
     return r == CUDA_SUCCESS;
 }
 
-template <int CG, bool A_MN, bool B_MN, bool BF16, typename OutT>
+template <int CG, bool MC, bool A_MN, bool B_MN, bool BF16, typename OutT>
 int launch_variant(TcParams& tp, const DeviceInfo& dev, cudaStream_t stream) {
     using C_ = Cfg<CG>;
-    auto kern = gemm_tc_kernel<CG, A_MN, B_MN, BF16, OutT>;
+    constexpr int CLUSTER = MC ? 2 * CG : CG;
+    auto kern = gemm_tc_kernel<CG, MC, A_MN, B_MN, BF16, OutT>;
     static std::mutex mu;
     static uint64_t configured = 0;   // bit per device
     static int max_clusters[64];
+    auto cluster_cfg = [&](cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int nclusters) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CLUSTER;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(CLUSTER * nclusters);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = C_::SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    };
     {
         std::lock_guard<std::mutex> lock(mu);
         const uint64_t bit = 1ull << (dev.device & 63);
@@ -501,19 +538,11 @@ int launch_variant(TcParams& tp, const DeviceInfo& dev, cudaStream_t stream) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C_::SMEM_BYTES) != cudaSuccess)
                 return kCuda;
-            int n = dev.sm_count / CG;
-            if (CG == 2) {
+            int n = dev.sm_count / CLUSTER;
+            if (CLUSTER > 1) {
                 cudaLaunchConfig_t cfg = {};
                 cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = CG;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.gridDim = dim3(CG * n);
-                cfg.blockDim = dim3(THREADS);
-                cfg.dynamicSmemBytes = C_::SMEM_BYTES;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
+                cluster_cfg(cfg, attr, n);
                 int q = 0;
                 if (cudaOccupancyMaxActiveClusters(&q, kern, &cfg) == cudaSuccess && q > 0)
                     n = q;
@@ -524,45 +553,38 @@ int launch_variant(TcParams& tp, const DeviceInfo& dev, cudaStream_t stream) {
             configured |= bit;
         }
     }
-    const int total = tp.tiles_m * tp.tiles_n;
+    const int unit_rows = MC ? (tp.tiles_m + 1) / 2 : tp.tiles_m;
+    const int total = unit_rows * tp.tiles_n;
     int nclusters = max_clusters[dev.device & 63];
     if (nclusters > total) nclusters = total;
     if (nclusters < 1) nclusters = 1;
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(CG * nclusters);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = C_::SMEM_BYTES;
+    cluster_cfg(cfg, attr, nclusters);
     cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, kern, tp) != cudaSuccess) return kCuda;
     note_launch();
     return kOk;
 }
 
-template <int CG, bool BF16, typename OutT>
+template <int CG, bool MC, bool BF16, typename OutT>
 int dispatch_majors(TcParams& tp, bool a_mn, bool b_mn, const DeviceInfo& dev,
                     cudaStream_t s) {
-    if (!a_mn && !b_mn) return launch_variant<CG, false, false, BF16, OutT>(tp, dev, s);
-    if (!a_mn && b_mn) return launch_variant<CG, false, true, BF16, OutT>(tp, dev, s);
-    if (a_mn && !b_mn) return launch_variant<CG, true, false, BF16, OutT>(tp, dev, s);
-    return launch_variant<CG, true, true, BF16, OutT>(tp, dev, s);
+    if (!a_mn && !b_mn) return launch_variant<CG, MC, false, false, BF16, OutT>(tp, dev, s);
+    if (!a_mn && b_mn) return launch_variant<CG, MC, false, true, BF16, OutT>(tp, dev, s);
+    if (a_mn && !b_mn) return launch_variant<CG, MC, true, false, BF16, OutT>(tp, dev, s);
+    return launch_variant<CG, MC, true, true, BF16, OutT>(tp, dev, s);
 }
 
-template <int CG>
+template <int CG, bool MC>
 int dispatch_types(TcParams& tp, int dtype, bool a_mn, bool b_mn, const DeviceInfo& dev,
                    cudaStream_t s) {
     switch (dtype) {
-        case 1: return dispatch_majors<CG, false, float>(tp, a_mn, b_mn, dev, s);
-        case 2: return dispatch_majors<CG, true, float>(tp, a_mn, b_mn, dev, s);
-        case 3: return dispatch_majors<CG, false, __half>(tp, a_mn, b_mn, dev, s);
-        case 4: return dispatch_majors<CG, true, __nv_bfloat16>(tp, a_mn, b_mn, dev, s);
+        case 1: return dispatch_majors<CG, MC, false, float>(tp, a_mn, b_mn, dev, s);
+        case 2: return dispatch_majors<CG, MC, true, float>(tp, a_mn, b_mn, dev, s);
+        case 3: return dispatch_majors<CG, MC, false, __half>(tp, a_mn, b_mn, dev, s);
+        case 4: return dispatch_majors<CG, MC, true, __nv_bfloat16>(tp, a_mn, b_mn, dev, s);
         default: return kInvalidArg;
     }
 }
@@ -570,10 +592,11 @@ int dispatch_types(TcParams& tp, int dtype, bool a_mn, bool b_mn, const DeviceIn
 }  // namespace
 
 int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
-                   uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled,
+                   uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled, int multicast,
                    cudaStream_t stream) {
     if (!get_encoder()) return kCuda;
     const int CG = cta_group == 1 ? 1 : 2;
+    const bool mc = CG == 2 && multicast;
     const bool bf16 = pr.dtype == 2 || pr.dtype == 4;
     const int tile_m = ROWS_A * CG;
     const int b_rows = TILE_N / CG;
@@ -581,11 +604,12 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     TcParams tp;
     std::memset(&tp, 0, sizeof(tp));
     // A: K-major -> dims {K, M}, box {64, 128}; M-major -> dims {M, K}, box {64, 64}.
+    // B likewise with its rows per CTA (64 per load when multicast).
     bool ok = pr.a_kmajor
         ? encode_2d(&tp.tmap_a, bf16, pr.A, pr.K, pr.M, pr.lda, BK, ROWS_A)
         : encode_2d(&tp.tmap_a, bf16, pr.A, pr.M, pr.K, pr.lda, 64, BK);
     ok = ok && (pr.b_kmajor
-        ? encode_2d(&tp.tmap_b, bf16, pr.B, pr.K, pr.N, pr.ldb, BK, b_rows)
+        ? encode_2d(&tp.tmap_b, bf16, pr.B, pr.K, pr.N, pr.ldb, BK, mc ? 64 : b_rows)
         : encode_2d(&tp.tmap_b, bf16, pr.B, pr.N, pr.K, pr.ldb, 64, BK));
     if (!ok) return kCuda;
 
@@ -624,8 +648,11 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     tp.fault_inject = fault_inject;
     if ((int64_t)tp.tiles_m * tp.tiles_n > 0x7fffffffLL) return kUnsupported;
 
-    return CG == 1 ? dispatch_types<1>(tp, pr.dtype, !pr.a_kmajor, !pr.b_kmajor, dev, stream)
-                   : dispatch_types<2>(tp, pr.dtype, !pr.a_kmajor, !pr.b_kmajor, dev, stream);
+    if (CG == 1)
+        return dispatch_types<1, false>(tp, pr.dtype, !pr.a_kmajor, !pr.b_kmajor, dev, stream);
+    if (mc)
+        return dispatch_types<2, true>(tp, pr.dtype, !pr.a_kmajor, !pr.b_kmajor, dev, stream);
+    return dispatch_types<2, false>(tp, pr.dtype, !pr.a_kmajor, !pr.b_kmajor, dev, stream);
 }
 
 }  // namespace libgemm

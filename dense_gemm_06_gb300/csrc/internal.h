@@ -38,9 +38,10 @@ int launch_sgemm_f32(const Problem& p, const DeviceInfo& dev, int config, cudaSt
 int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
                          int64_t cols, const DeviceInfo& dev, cudaStream_t stream);
 // c_tma_enabled: 1 = store C with TMA when its rows are 16-byte aligned,
-// 0 = always use the st.global epilogue.
+// 0 = always use the st.global epilogue. multicast: 1 = clusters of two CTA
+// pairs sharing B through TMA multicast (2-CTA mode only).
 int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, int cta_group,
-                   uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled,
+                   uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled, int multicast,
                    cudaStream_t stream);
 
 void note_launch(uint64_t n = 1);

@@ -123,6 +123,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint3
     }
 }
 
+// 2-D tiled TMA load multicast to every CTA of `mask` (same shared-memory
+// offset in each). With .cta_group::2 the completion goes to the barrier at
+// the offset of `bar` in the pair leader (even rank) of each destination.
+__device__ __forceinline__ void tma_load_2d_mc_pair(uint32_t dst, const void* map, uint32_t bar,
+                                                    int32_t x, int32_t y, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;"
+        :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "h"(mask) : "memory");
+}
+
 // 2-D tiled TMA store from this CTA's shared memory (bulk async-group).
 __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"

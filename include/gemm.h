@@ -220,7 +220,12 @@ enum gemm_option {
        of each 32 x 32 chunk that lies entirely inside C when C's base and
        row pitch are 16-byte aligned; row-coalesced st.global for the other
        chunks), 1 = always st.global. */
-    GEMM_OPT_TC_STORE = 6
+    GEMM_OPT_TC_STORE = 6,
+    /* Operand multicast in the 2-CTA tensor-core kernel: 0 = automatic
+       (currently off), 1 = off, 2 = on: clusters of two CTA pairs compute
+       vertically adjacent 256 x 256 tiles and each half of the shared B tile
+       is loaded once per cluster and multicast by TMA to both pairs. */
+    GEMM_OPT_TC_MULTICAST = 7
 };
 
 /* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */

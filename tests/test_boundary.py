@@ -46,7 +46,8 @@ def test_enums_match_header():
                  "GEMM_F16_F16", "GEMM_BF16_BF16", "GEMM_OK", "GEMM_ERR_INVALID_ARG",
                  "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
                  "GEMM_OPT_WAIT_LIMIT_NS", "GEMM_OPT_TC_CTA_GROUP", "GEMM_OPT_TC_FAULT_INJECT",
-                 "GEMM_OPT_SIMT_CONFIG", "GEMM_OPT_SIMT_TRANSPOSE", "GEMM_OPT_TC_STORE"):
+                 "GEMM_OPT_SIMT_CONFIG", "GEMM_OPT_SIMT_TRANSPOSE", "GEMM_OPT_TC_STORE",
+                 "GEMM_OPT_TC_MULTICAST"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m, name
         assert int(m.group(1)) == getattr(lg, name), name
@@ -132,6 +133,8 @@ def test_strerror_and_options(lib):
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_TRANSPOSE, 3) == lg.GEMM_ERR_INVALID_ARG
     assert lg.gemm_get_option(lg.GEMM_OPT_TC_STORE) == 0
     assert lg.gemm_set_option(lg.GEMM_OPT_TC_STORE, 2) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_get_option(lg.GEMM_OPT_TC_MULTICAST) == 0
+    assert lg.gemm_set_option(lg.GEMM_OPT_TC_MULTICAST, 3) == lg.GEMM_ERR_INVALID_ARG
 
 
 def test_launch_count_unchanged_by_rejected_calls(lib):

@@ -75,13 +75,14 @@ def test_fp32_8192_cubed_all_majors(fp32_8192_logical, am, bm):
                   what=f"8192^3 fp32 A{'KM'[am]} B{'KN'[bm]}", seed=1027)
 
 
-@pytest.mark.parametrize("cta_group", [0, 1])
-def test_bf16_8192_cubed(cta_group):
+@pytest.mark.parametrize("cta_group,multicast", [(0, 0), (1, 0), (2, 2)])
+def test_bf16_8192_cubed(cta_group, multicast):
     n = 8192
     A, lda, B, ldb = make_operands(n, n, n, lg.GEMM_BF16_BF16, 0, 0, "normal", 1028)
-    C = run_device_gemm(n, n, n, lg.GEMM_BF16_BF16, A, lda, 0, B, ldb, 0, cta_group=cta_group)
+    C = run_device_gemm(n, n, n, lg.GEMM_BF16_BF16, A, lda, 0, B, ldb, 0, cta_group=cta_group,
+                        multicast=multicast)
     check_sampled(C, n, n, n, lg.GEMM_BF16_BF16, A, lda, 0, B, ldb, 0, exact=False,
-                  what=f"8192^3 bf16 (cg={cta_group})", seed=1028)
+                  what=f"8192^3 bf16 (cg={cta_group}, mc={multicast})", seed=1028)
 
 
 def test_fp16_int_4095x3071x1037_ragged_bit_exact():
