@@ -66,6 +66,10 @@ def _load():
             lib.oracle_f32_to_f64.restype = ctypes.c_double
             lib.oracle_f32_to_f64.argtypes = [ctypes.c_uint32]
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_epilogue.restype = ctypes.c_int
+            lib.oracle_epilogue.argtypes = [i64, i64, p, p, i64, p, i64, ctypes.c_double,
+                                            ctypes.c_double, p, i64, ctypes.c_int, ctypes.c_int,
+                                            p, ctypes.c_int, p]
             _lib = lib
     return _lib
 
@@ -119,3 +123,32 @@ def gemm_ref(M: int, N: int, K: int,
     if rc != 0:
         raise ValueError(f"oracle_gemm rejected the arguments (status {rc})")
     return C, S
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
+
+
+def epilogue_ref(M: int, N: int, C_ref: np.ndarray, alpha: float, beta: float,
+                 C_in=None, ldc: int = 0, c_major: int = 1, c_dtype: str = "f32",
+                 bias=None, act: str = "none", rows=None, cols=None) -> np.ndarray:
+    """D = act(alpha * C_ref + beta * C_in + bias) in fp64 for the block of
+    C_ref (the same rows/cols lists given to gemm_ref); see gemm_oracle.c."""
+    lib = _load()
+    C_ref = np.ascontiguousarray(C_ref, dtype=np.float64)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else len(r)
+    nc = N if c is None else len(c)
+    D = np.zeros((nr, nc), dtype=np.float64)
+    if nr == 0 or nc == 0:
+        return D
+    cin = None if C_in is None else np.ascontiguousarray(C_in)
+    b = None if bias is None else np.ascontiguousarray(bias)
+    rc = lib.oracle_epilogue(M, N, C_ref.ctypes.data,
+                             None if r is None else r.ctypes.data, nr,
+                             None if c is None else c.ctypes.data, nc,
+                             float(alpha), float(beta), _ptr(cin), ldc, c_major,
+                             DTYPES[c_dtype], _ptr(b), ACTIVATIONS[act], D.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_epilogue rejected the arguments (status {rc})")
+    return D

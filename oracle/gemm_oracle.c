@@ -241,3 +241,45 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K,
     free(bcols);
     return ORACLE_OK;
 }
+
+/*
+ * oracle_epilogue: D = act(alpha * C_ref + beta * C_in + bias), elementwise in
+ * fp64, for the block whose C_ref was computed by oracle_gemm (n_rows x
+ * n_cols, row-major; rows/cols are the same index lists, NULL = all).
+ *   C_in   : the incoming C (storage of c_dtype, addressed with ldc/c_major as
+ *            the C ABI does: c_major 1 = C[m*ldc+n], 0 = C[n*ldc+m]); read
+ *            only when beta != 0
+ *   bias   : NULL or N elements of c_dtype, bias[n] added to column n
+ *   act    : 0 none, 1 ReLU max(x, 0), 2 GELU x * Phi(x) = x/2 (1 + erf(x/sqrt 2))
+ * This is the fused epilogue of the CuTe DSL Ampere SGEMM example (its
+ * `epilogue_op` hook, applied to the accumulator before the store) with the
+ * usual GEMM scaling, bias and activation written out.
+ */
+int oracle_epilogue(int64_t M, int64_t N, const double *C_ref,
+                    const int64_t *rows, int64_t n_rows, const int64_t *cols, int64_t n_cols,
+                    double alpha, double beta, const void *C_in, int64_t ldc, int c_major,
+                    int c_dtype, const void *bias, int act, double *D_out) {
+    if (!rows) n_rows = M;
+    if (!cols) n_cols = N;
+    if (n_rows < 0 || n_cols < 0 || !C_ref || !D_out) return ORACLE_EINVAL;
+    if (c_dtype < 0 || c_dtype > 2 || act < 0 || act > 2) return ORACLE_EINVAL;
+    if (beta != 0.0 && !C_in) return ORACLE_EINVAL;
+    /* C viewed as an operand: row-major C is "K-major" with r = m, k = n */
+    operand_t oc = {C_in, ldc, c_major == 1 ? ORACLE_MAJOR_K : ORACLE_MAJOR_MN, c_dtype};
+    operand_t ob = {bias, 0, ORACLE_MAJOR_MN, c_dtype};
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        if (m < 0 || m >= M) return ORACLE_EINVAL;
+        for (int64_t j = 0; j < n_cols; ++j) {
+            int64_t n = cols ? cols[j] : j;
+            if (n < 0 || n >= N) return ORACLE_EINVAL;
+            double x = alpha * C_ref[i * n_cols + j];
+            if (beta != 0.0) x += beta * element(&oc, m, n);
+            if (bias) x += element(&ob, n, 0); /* bias[n]: MN-major, r = n, k = 0 */
+            if (act == 1) x = x > 0.0 ? x : 0.0;
+            else if (act == 2) x = 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+            D_out[i * n_cols + j] = x;
+        }
+    }
+    return ORACLE_OK;
+}

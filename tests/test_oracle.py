@@ -318,3 +318,60 @@ def _mutant(kind):
 def test_pins_catch_planted_mistakes(kind):
     with np.errstate(all="ignore"):
         assert run_pins(_mutant(kind)), f"no pin caught the planted mistake {kind!r}"
+
+
+# ------------------------------------------------------ fused epilogue --
+# D = act(alpha * C + beta * C_in + bias): the CuTe Ampere SGEMM example's
+# epilogue_op hook with scaling, bias and activation written out.
+
+def test_epilogue_pins():
+    rng = np.random.default_rng(3)
+    M, N = 5, 7
+    C = rng.integers(-50, 50, (M, N)).astype(np.float64)
+    # identity
+    assert np.array_equal(oracle.epilogue_ref(M, N, C, 1.0, 0.0), C)
+    # scaling only
+    assert np.array_equal(oracle.epilogue_ref(M, N, C, -0.5, 0.0), -0.5 * C)
+    # bias broadcast along rows, indexed by the column
+    bias = np.arange(N, dtype=np.float32) * 3 - 4
+    D = oracle.epilogue_ref(M, N, C, 1.0, 0.0, bias=bias)
+    assert np.array_equal(D - C, np.broadcast_to(bias.astype(np.float64), (M, N)))
+    # beta * C_in in both layouts of C (and 16-bit storage), dyadic => exact
+    Lc = rng.integers(-8, 8, (M, N)).astype(np.float64)
+    row_major = np.full(M * (N + 2), np.nan, np.float32).reshape(M, N + 2)
+    row_major[:, :N] = Lc
+    col_major = np.full(N * (M + 1), np.nan, np.float32).reshape(N, M + 1)
+    col_major[:, :M] = Lc.T
+    D1 = oracle.epilogue_ref(M, N, C, 1.0, 0.25, C_in=row_major.ravel(), ldc=N + 2, c_major=1)
+    D0 = oracle.epilogue_ref(M, N, C, 1.0, 0.25, C_in=col_major.ravel(), ldc=M + 1, c_major=0)
+    assert np.array_equal(D1, C + 0.25 * Lc) and np.array_equal(D0, D1)
+    bf = datagen.to_storage(Lc.ravel(), "bf16")
+    D2 = oracle.epilogue_ref(M, N, C, 1.0, 0.25, C_in=bf, ldc=N, c_major=1, c_dtype="bf16")
+    assert np.array_equal(D2, D1)
+    # beta == 0 never reads C_in (NaN storage must not leak in)
+    nan_c = np.full(M * N, np.nan, np.float32)
+    assert np.array_equal(oracle.epilogue_ref(M, N, C, 1.0, 0.0, C_in=nan_c, ldc=N), C)
+    # ReLU
+    assert np.array_equal(oracle.epilogue_ref(M, N, C, 1.0, 0.0, act="relu"), np.maximum(C, 0))
+    # GELU: x * Phi(x); Phi(1) = 0.8413447460685429 (normal table), odd part = x
+    g = oracle.epilogue_ref(1, 5, np.array([[1.0, -1.0, 0.0, 10.0, -10.0]]), 1.0, 0.0,
+                            act="gelu")[0]
+    assert abs(g[0] - 0.8413447460685429) < 1e-15
+    assert abs(g[1] + (1 - 0.8413447460685429)) < 1e-15
+    assert g[2] == 0.0 and abs(g[3] - 10.0) < 1e-15 and abs(g[4]) < 1e-15
+    assert abs((g[0] - g[1]) - 1.0) < 1e-15
+    # sampled block equals the same block of the full result
+    rows, cols = np.array([4, 0]), np.array([6, 2, 3])
+    Db = oracle.epilogue_ref(M, N, C[np.ix_(rows, cols)], 2.0, 0.25, C_in=row_major.ravel(),
+                             ldc=N + 2, c_major=1, bias=bias, act="relu", rows=rows, cols=cols)
+    Df = oracle.epilogue_ref(M, N, C, 2.0, 0.25, C_in=row_major.ravel(), ldc=N + 2,
+                             c_major=1, bias=bias, act="relu")
+    assert np.array_equal(Db, Df[np.ix_(rows, cols)])
+
+
+def test_epilogue_rejects_bad_arguments():
+    C = np.zeros((2, 2))
+    with pytest.raises(ValueError):
+        oracle.epilogue_ref(2, 2, C, 1.0, 0.5)              # beta != 0 without C_in
+    with pytest.raises(ValueError):
+        oracle.epilogue_ref(2, 2, C, 1.0, 0.0, rows=[2])    # row out of range
