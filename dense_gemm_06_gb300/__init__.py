@@ -30,6 +30,13 @@ GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA, GEMM_ERR_TIM
 GEMM_OPT_WAIT_LIMIT_NS, GEMM_OPT_TC_CTA_GROUP, GEMM_OPT_TC_FAULT_INJECT = 1, 2, 3
 GEMM_OPT_SIMT_CONFIG, GEMM_OPT_SIMT_TRANSPOSE, GEMM_OPT_TC_STORE = 4, 5, 6
 GEMM_OPT_TC_MULTICAST = 7
+GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_GELU = 0, 1, 2
+
+
+class GemmEpilogue(ctypes.Structure):
+    """struct gemm_epilogue: D = act(alpha * A B^T + beta * C + bias)."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("bias", ctypes.c_void_p), ("activation", ctypes.c_int)]
 
 # storage type of A/B and of C per dtype
 IN_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f16", GEMM_BF16_F32: "bf16",
@@ -37,7 +44,7 @@ IN_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f16", GEMM_BF16_F32: "bf16",
 OUT_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f32", GEMM_BF16_F32: "f32",
             GEMM_F16_F16: "f16", GEMM_BF16_BF16: "bf16"}
 
-EXPORTS = ("gemm", "gemm_host", "gemm_noalloc", "gemm_strerror", "gemm_check_device_error",
+EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_noalloc", "gemm_strerror", "gemm_check_device_error",
            "gemm_release_workspace", "gemm_launch_count", "gemm_set_option",
            "gemm_get_option")
 
@@ -67,6 +74,8 @@ def load(path: str = LIB_PATH):
         for name in ("gemm", "gemm_host", "gemm_noalloc"):
             f = getattr(lib, name)
             f.restype, f.argtypes = ci, sig
+        lib.gemm_ex.restype = ci
+        lib.gemm_ex.argtypes = sig[:-1] + [ctypes.POINTER(GemmEpilogue), vp]
         lib.gemm_strerror.restype, lib.gemm_strerror.argtypes = ctypes.c_char_p, [ci]
         lib.gemm_check_device_error.restype = ci
         lib.gemm_check_device_error.argtypes = [vp]
@@ -108,6 +117,14 @@ def gemm(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype, stre
     """C = A * B^T on device buffers; returns the gemm_status."""
     return load().gemm(M, N, K, _ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C), ldc,
                        c_major, dtype, _stream(stream))
+
+
+def gemm_ex(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype,
+            alpha=1.0, beta=0.0, bias=None, activation=GEMM_ACT_NONE, stream=None) -> int:
+    """C = act(alpha * A B^T + beta * C + bias[n]); see include/gemm.h."""
+    epi = GemmEpilogue(alpha, beta, _ptr(bias) or None, activation)
+    return load().gemm_ex(M, N, K, _ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C), ldc,
+                          c_major, dtype, ctypes.byref(epi), _stream(stream))
 
 
 def gemm_host(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype,

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "../../include/gemm.h"
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace libgemm {
@@ -201,10 +202,10 @@ Problem normalise(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, i
     Problem p;
     if (c_major == GEMM_MAJOR_MN) {
         p = {M, N, K, A, lda, a_major == GEMM_MAJOR_K, B, ldb, b_major == GEMM_MAJOR_K, C, ldc,
-             dtype};
+             dtype, EpiParams{}};
     } else {
         p = {N, M, K, B, ldb, b_major == GEMM_MAJOR_K, A, lda, a_major == GEMM_MAJOR_K, C, ldc,
-             dtype};
+             dtype, EpiParams{}};
     }
     return p;
 }
@@ -294,6 +295,39 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_
 
 void note_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+namespace {
+
+// C = act(beta * C + bias) for K == 0 (the product term is zero).
+template <typename OutT>
+__global__ void epilogue_only_kernel(OutT* C, int64_t ldc, int rows, int cols, EpiParams e) {
+    const int64_t total = (int64_t)rows * cols;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / cols), c = (int)(i - (int64_t)r * cols);
+        OutT* d = C + (int64_t)r * ldc + c;
+        const float old = e.beta != 0.f ? to_f32(*d) : 0.f;
+        *d = from_f32<OutT>(epilogue_value<OutT>(e, 0.f, old, r, c));
+    }
+}
+
+}  // namespace
+
+int launch_epilogue_only(const Problem& p, const DeviceInfo& dev, cudaStream_t s) {
+    const int grid = grid_for(p.M * p.N, dev);
+    if (out_bytes(p.dtype) == 4)
+        epilogue_only_kernel<float><<<grid, 256, 0, s>>>(static_cast<float*>(p.C), p.ldc,
+                                                          (int)p.M, (int)p.N, p.epi);
+    else if (p.dtype == GEMM_BF16_BF16)
+        epilogue_only_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            static_cast<__nv_bfloat16*>(p.C), p.ldc, (int)p.M, (int)p.N, p.epi);
+    else
+        epilogue_only_kernel<__half><<<grid, 256, 0, s>>>(static_cast<__half*>(p.C), p.ldc,
+                                                           (int)p.M, (int)p.N, p.epi);
+    if (cudaGetLastError() != cudaSuccess) return kCuda;
+    note_launch();
+    return kOk;
+}
+
 int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
                const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
                int dtype) {
@@ -335,6 +369,38 @@ int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_majo
         const Problem p =
             normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
         return run_device(p, *dev, pool, static_cast<cudaStream_t>(stream));
+    } catch (...) {
+        return kCuda;
+    }
+}
+
+int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+            const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major, int dtype,
+            const gemm_epilogue* epi, void* stream) {
+    try {
+        if (!epi)
+            return gemm(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype, stream);
+        int rc = validate(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+        if (rc != kOk) return rc;
+        if (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU) return kInvalidArg;
+        if (epi->bias && reinterpret_cast<uintptr_t>(epi->bias) % out_bytes(dtype))
+            return kInvalidArg;
+        if (M == 0 || N == 0) return kOk;
+        const bool plain = epi->alpha == 1.f && epi->beta == 0.f && !epi->bias &&
+                           epi->activation == GEMM_ACT_NONE;
+        if (plain)
+            return gemm(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype, stream);
+        DeviceInfo* dev = nullptr;
+        cudaMemPool_t pool = nullptr;
+        rc = current_device(&dev, &pool);
+        if (rc != kOk) return rc;
+        Problem p = normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+        // a column-major C is stored transposed: its columns are our rows
+        p.epi = EpiParams{1, epi->alpha, epi->beta, epi->bias, c_major == GEMM_MAJOR_K ? 1 : 0,
+                          epi->activation};
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (K == 0) return launch_epilogue_only(p, *dev, s);
+        return run_device(p, *dev, pool, s);
     } catch (...) {
         return kCuda;
     }

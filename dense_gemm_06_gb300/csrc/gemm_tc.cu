@@ -44,6 +44,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx_sm100.cuh"
 
@@ -92,6 +93,7 @@ struct TcParams {
     unsigned int* err;         // device error word
     unsigned long long wait_limit_ns;
     int fault_inject;          // test hook: 1 = epilogue waits on a barrier nobody arrives at
+    EpiParams epi;             // fused epilogue (inactive for a plain GEMM)
 };
 
 struct TileCoord {
@@ -175,6 +177,68 @@ __device__ __forceinline__ int swz(int r) {
     else return (r >> 1) & 3;
 }
 
+// The chunk with the fused epilogue: the fp32 accumulators are staged as is
+// (128-byte rows, 128-byte swizzle pattern) and the epilogue is applied while
+// reading the tile back row-wise, so C_old, bias and the store are coalesced
+// and a 16-bit C is rounded once, after the epilogue.
+template <typename OutT>
+__device__ __forceinline__ void store_chunk_epi(const TcParams& p, uint32_t stage, int lane,
+                                                int row0, int col0, const uint32_t (&v)[32]) {
+    const uint32_t my_row = stage + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        sts128(my_row + (uint32_t)((u ^ (lane & 7)) * 16), v[4 * u], v[4 * u + 1], v[4 * u + 2],
+               v[4 * u + 3]);
+    __syncwarp();
+    const int u = lane & 7;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int r = 4 * j + (lane >> 3);
+        const uint4 raw = lds128(stage + (uint32_t)r * 128u + (uint32_t)((u ^ (r & 7)) * 16));
+        float f[4] = {__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
+                      __uint_as_float(raw.w)};
+        const int grow = row0 + r, gcol = col0 + 4 * u;
+        if (grow >= p.M) continue;
+        OutT* dst = static_cast<OutT*>(p.C) + (int64_t)grow * p.ldc + gcol;
+        if (p.c_vec && gcol + 3 < p.N) {
+            float old[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (sizeof(OutT) == 4) {
+                if (p.epi.beta != 0.f) {
+                    const float4 o = *reinterpret_cast<const float4*>(dst);
+                    old[0] = o.x; old[1] = o.y; old[2] = o.z; old[3] = o.w;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    f[e] = epilogue_value<OutT>(p.epi, f[e], old[e], grow, gcol + e);
+                *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+            } else {
+                if (p.epi.beta != 0.f) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) old[e] = to_f32(dst[e]);
+                }
+                OutT o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    o[e] = from_f32<OutT>(epilogue_value<OutT>(p.epi, f[e], old[e], grow, gcol + e));
+                uint2 pk;
+                pk.x = (uint32_t)(*reinterpret_cast<uint16_t*>(&o[0])) |
+                       ((uint32_t)(*reinterpret_cast<uint16_t*>(&o[1])) << 16);
+                pk.y = (uint32_t)(*reinterpret_cast<uint16_t*>(&o[2])) |
+                       ((uint32_t)(*reinterpret_cast<uint16_t*>(&o[3])) << 16);
+                *reinterpret_cast<uint2*>(dst) = pk;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (gcol + e >= p.N) continue;
+                const float old = p.epi.beta != 0.f ? to_f32(dst[e]) : 0.f;
+                dst[e] = from_f32<OutT>(epilogue_value<OutT>(p.epi, f[e], old, grow, gcol + e));
+            }
+        }
+    }
+    __syncwarp();  // the tile is rewritten by the next chunk
+}
+
 // Writes one 32 x 32 chunk of C: thread `lane` holds row (row0 + lane),
 // columns col0 .. col0+31 in v[]. The chunk goes through the warp's staging
 // tile and leaves it either by one TMA store (C rows 16-byte aligned and the
@@ -186,6 +250,10 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
                                             int col0, const uint32_t (&v)[32]) {
     constexpr int ES = (int)sizeof(OutT);
     constexpr int ROW_BYTES = 32 * ES;
+    if (p.epi.active) {
+        store_chunk_epi<OutT>(p, stage, lane, row0, col0, v);
+        return;
+    }
     if (p.c_tma) {
         // the previous chunk's TMA store must have finished reading the tile
         if (lane == 0) bulk_wait_read_all();
@@ -617,8 +685,9 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     // C through TMA when its base and rows are 16-byte aligned: box 32 x 32,
     // the staging tile's swizzle (128-byte rows for fp32, 64-byte for 16-bit).
     tp.c_tma = 0;
+    tp.epi = pr.epi;  // an active epilogue reads/stores C itself (no TMA store)
     if ((reinterpret_cast<uintptr_t>(pr.C) & 15u) == 0 && ((pr.ldc * out_bytes) & 15) == 0 &&
-        c_tma_enabled) {
+        c_tma_enabled && !pr.epi.active) {
         const cuuint64_t dims[2] = {(cuuint64_t)pr.N, (cuuint64_t)pr.M};
         const cuuint64_t strides[1] = {(cuuint64_t)(pr.ldc * out_bytes)};
         const cuuint32_t box[2] = {32, 32};

@@ -7,6 +7,16 @@
 
 namespace libgemm {
 
+// Fused epilogue D = act(alpha * acc + beta * C_old + bias) (gemm_ex); passed
+// by value to the kernels.
+struct EpiParams {
+    int active;        // 0: plain store of the accumulator
+    float alpha, beta;
+    const void* bias;  // C's element type; may be null
+    int bias_rows;     // 1: bias indexed by the row of the stored (normalised) C
+    int act;           // 0 none, 1 ReLU, 2 GELU
+};
+
 // A problem after layout normalisation: C is always row-major (N-major) with
 // leading dimension ldc; A is M x K and B is N x K, each K- or MN-major.
 struct Problem {
@@ -20,6 +30,7 @@ struct Problem {
     void* C;
     int64_t ldc;
     int dtype;  // gemm_dtype
+    EpiParams epi;
 };
 
 struct DeviceInfo {
@@ -55,6 +66,10 @@ Problem normalised(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
                    const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
                    int dtype);
 int error_word_address(unsigned int** out);
+
+// C = act(beta * C + bias) in place (the K == 0 case of gemm_ex), rows x cols
+// of the normalised row-major C.
+int launch_epilogue_only(const Problem& p, const DeviceInfo& dev, cudaStream_t stream);
 
 // Status codes shared with the public header (kept numerically identical).
 enum : int {

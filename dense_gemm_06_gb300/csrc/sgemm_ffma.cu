@@ -22,6 +22,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace libgemm {
@@ -58,6 +59,7 @@ struct SgemmParams {
     int M, N, K;
     int tiles_m, tiles_n;
     int c_vec;
+    EpiParams epi;  // fused epilogue (inactive for a plain GEMM)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -264,8 +266,24 @@ __global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const Sg
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = n0 + tx * 4 + h * 64;
-            const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
-                                acc[i][2 * h + 1].y};
+            float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                          acc[i][2 * h + 1].y};
+            if (p.epi.active) {  // D = act(alpha * acc + beta * C_old + bias)
+                float old[4] = {0.f, 0.f, 0.f, 0.f};
+                if (p.epi.beta != 0.f) {
+                    if (p.c_vec && col + 3 < p.N) {
+                        const float4 o = *reinterpret_cast<const float4*>(crow + col);
+                        old[0] = o.x; old[1] = o.y; old[2] = o.z; old[3] = o.w;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (col + j < p.N) old[j] = crow[col + j];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < p.N) v[j] = epilogue_value<float>(p.epi, v[j], old[j], row, col + j);
+            }
             if (p.c_vec && col + 3 < p.N) {
                 *reinterpret_cast<float4*>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
@@ -379,6 +397,7 @@ int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, cudaS
     sp.tiles_m = (int)((pr.M + BM - 1) / BM);
     sp.tiles_n = (int)((pr.N + BN - 1) / BN);
     sp.c_vec = aligned16(pr.C, pr.ldc) ? 1 : 0;
+    sp.epi = pr.epi;
     if ((int64_t)sp.tiles_m * sp.tiles_n > 0x7fffffffLL) return kUnsupported;
 
     // A/B variant: K-major (4-byte transposing copies), MN-major 16-byte or 4-byte.

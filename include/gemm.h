@@ -111,6 +111,39 @@ int gemm(int64_t M, int64_t N, int64_t K,
          void *C, int64_t ldc, int c_major,
          int dtype, void *stream);
 
+/* Activations of the fused epilogue. */
+enum gemm_activation {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1, /* max(x, 0) */
+    GEMM_ACT_GELU = 2  /* x * Phi(x) = x / 2 * (1 + erf(x / sqrt(2))) */
+};
+
+/* Fused epilogue of gemm_ex: D = act(alpha * (A * B^T) + beta * C + bias). */
+typedef struct gemm_epilogue {
+    float alpha;      /* scale of the product */
+    float beta;       /* scale of the incoming C; 0 = C is not read */
+    const void *bias; /* NULL, or a DEVICE vector of C's element type with one
+                         entry per column of C (index n), 16-bit aligned */
+    int activation;   /* enum gemm_activation */
+} gemm_epilogue;
+
+/*
+ * gemm_ex -- C = act(alpha * A * B^T + beta * C + bias[n]) in one pass: the
+ * accumulator (fp32) goes through the epilogue in fp32 registers before C is
+ * rounded to its type and stored. This is the CuTe DSL Ampere SGEMM example's
+ * `epilogue_op` hook (applied to the accumulator before the store), with
+ * scaling, bias and activation. `epi` == NULL, or alpha 1 / beta 0 / no bias
+ * / no activation, is exactly gemm(). With beta != 0, C is read before it is
+ * overwritten (it must hold valid data). K == 0 gives act(beta * C + bias).
+ * Arguments, layouts, status codes and asynchrony are those of gemm(); an
+ * unknown activation or a misaligned bias is GEMM_ERR_INVALID_ARG.
+ */
+int gemm_ex(int64_t M, int64_t N, int64_t K,
+            const void *A, int64_t lda, int a_major,
+            const void *B, int64_t ldb, int b_major,
+            void *C, int64_t ldc, int c_major,
+            int dtype, const gemm_epilogue *epi, void *stream);
+
 /*
  * gemm_host -- the same product with HOST buffers (pinned or pageable).
  * On `stream`: takes device buffers from the library's scratch pool (row

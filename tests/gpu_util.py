@@ -54,6 +54,21 @@ class CBuffer:
     def ptr(self) -> int:
         return int(self.dev.data_ptr()) + GUARD * self.esize
 
+    def fill(self, logical_storage: np.ndarray):
+        """Write a logical (M x N) matrix of C's storage type into the body
+        (padding and guard bands keep their canaries); returns the storage
+        array of the body as the C ABI addresses it."""
+        torch = torch_mod()
+        host = self.host_init.copy()
+        body = host[GUARD:GUARD + self.span]
+        L = logical_storage if self.c_major == lg.GEMM_MAJOR_MN else logical_storage.T
+        for r in range(self.outer):
+            body[r * self.ldc:r * self.ldc + self.inner] = L[r]
+        self.host_init = host  # canaries of padding/guards unchanged
+        src = host.view(np.int16) if host.dtype == np.uint16 else host
+        self.dev.copy_(torch.from_numpy(src.copy()).to(self.dev.device))
+        return body.copy()
+
     def read(self) -> np.ndarray:
         """Logical C (M x N, float64); asserts guard bands and padding intact."""
         raw = self.dev.cpu().numpy()

@@ -47,7 +47,7 @@ def test_enums_match_header():
                  "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
                  "GEMM_OPT_WAIT_LIMIT_NS", "GEMM_OPT_TC_CTA_GROUP", "GEMM_OPT_TC_FAULT_INJECT",
                  "GEMM_OPT_SIMT_CONFIG", "GEMM_OPT_SIMT_TRANSPOSE", "GEMM_OPT_TC_STORE",
-                 "GEMM_OPT_TC_MULTICAST"):
+                 "GEMM_OPT_TC_MULTICAST", "GEMM_ACT_NONE", "GEMM_ACT_RELU", "GEMM_ACT_GELU"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m, name
         assert int(m.group(1)) == getattr(lg, name), name
@@ -82,6 +82,16 @@ def test_valid_element_alignment_passes_validation(lib):
     # no usable sm_103 device the call then stops at the device check.
     rc = call(A=P + 2, B=P + 6, lda=7, ldb=5, C=P + 4, ldc=9, dtype=lg.GEMM_F16_F32)
     assert rc in (lg.GEMM_ERR_UNSUPPORTED, lg.GEMM_OK) or rc == lg.GEMM_ERR_CUDA
+
+
+def test_gemm_ex_host_checks(lib):
+    assert lg.gemm_ex(4, 4, 4, P, 4, 0, P, 4, 0, P, 4, 1, lg.GEMM_F32, activation=3) == \
+        lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_ex(4, 4, 4, P, 4, 0, P, 4, 0, P, 4, 1, lg.GEMM_F32, bias=P + 2) == \
+        lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_ex(-1, 4, 4, P, 4, 0, P, 4, 0, P, 4, 1, lg.GEMM_F32, beta=1.0) == \
+        lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_ex(0, 4, 4, P, 4, 0, P, 4, 0, P, 4, 1, lg.GEMM_F32, beta=1.0) == lg.GEMM_OK
 
 
 def test_degenerate_sizes_need_no_device(lib):
