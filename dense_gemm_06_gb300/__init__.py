@@ -33,6 +33,16 @@ GEMM_OPT_TC_MULTICAST = 7
 GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_GELU = 0, 1, 2
 
 
+class GemmTuning(ctypes.Structure):
+    """struct gemm_tuning: the configuration gemm_tune chose."""
+    _fields_ = [("simt_config", ctypes.c_int), ("simt_transpose", ctypes.c_int),
+                ("tc_cta_group", ctypes.c_int), ("tc_multicast", ctypes.c_int),
+                ("tc_store", ctypes.c_int), ("ms", ctypes.c_float), ("candidates", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
 class GemmEpilogue(ctypes.Structure):
     """struct gemm_epilogue: D = act(alpha * A B^T + beta * C + bias)."""
     _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float),
@@ -44,9 +54,9 @@ IN_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f16", GEMM_BF16_F32: "bf16",
 OUT_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f32", GEMM_BF16_F32: "f32",
             GEMM_F16_F16: "f16", GEMM_BF16_BF16: "bf16"}
 
-EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_noalloc", "gemm_strerror", "gemm_check_device_error",
-           "gemm_release_workspace", "gemm_launch_count", "gemm_set_option",
-           "gemm_get_option")
+EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_noalloc", "gemm_tune", "gemm_tune_reset",
+           "gemm_strerror", "gemm_check_device_error", "gemm_release_workspace",
+           "gemm_launch_count", "gemm_set_option", "gemm_get_option")
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +86,9 @@ def load(path: str = LIB_PATH):
             f.restype, f.argtypes = ci, sig
         lib.gemm_ex.restype = ci
         lib.gemm_ex.argtypes = sig[:-1] + [ctypes.POINTER(GemmEpilogue), vp]
+        lib.gemm_tune.restype = ci
+        lib.gemm_tune.argtypes = sig[:-1] + [ci, vp, ctypes.POINTER(GemmTuning)]
+        lib.gemm_tune_reset.restype, lib.gemm_tune_reset.argtypes = None, []
         lib.gemm_strerror.restype, lib.gemm_strerror.argtypes = ctypes.c_char_p, [ci]
         lib.gemm_check_device_error.restype = ci
         lib.gemm_check_device_error.argtypes = [vp]
@@ -140,6 +153,20 @@ def gemm_noalloc(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dty
     scratch inside the library); see include/gemm.h."""
     return load().gemm_noalloc(M, N, K, _ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C),
                                ldc, c_major, dtype, _stream(stream))
+
+
+def gemm_tune(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype,
+              iterations=5, stream=None):
+    """Measure every configuration for this problem, record the fastest;
+    returns (status, dict of the chosen configuration)."""
+    t = GemmTuning()
+    rc = load().gemm_tune(M, N, K, _ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C), ldc,
+                          c_major, dtype, iterations, _stream(stream), ctypes.byref(t))
+    return rc, t.as_dict()
+
+
+def gemm_tune_reset() -> None:
+    load().gemm_tune_reset()
 
 
 def gemm_strerror(status: int) -> str:

@@ -12,6 +12,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "../../include/gemm.h"
@@ -35,6 +36,36 @@ std::atomic<int> g_simt_config{0};
 std::atomic<int> g_simt_transpose{0};
 std::atomic<int> g_tc_store{0};
 std::atomic<int> g_tc_multicast{0};
+
+// The kernel configuration one call runs with. Every field is resolved
+// (no "automatic" values): an option set to a non-zero value wins, then a
+// gemm_tune() entry for the problem, then the built-in choice.
+struct RunConfig {
+    int simt_config;     // 1..6
+    int simt_transpose;  // 0 automatic size rule, 1 never, 2 always
+    int cta_group;       // 1 or 2
+    int multicast;       // 1 off, 2 on
+    int tc_store;        // 0 TMA where possible, 1 st.global
+};
+
+// Problems gemm_tune() has measured: shape, types, layouts and whether each
+// operand's base/pitch is 16-byte aligned (which changes the kernels run).
+struct TuneKey {
+    int64_t M, N, K;
+    int dtype, a_major, b_major, c_major, align;
+    bool operator<(const TuneKey& o) const {
+        if (M != o.M) return M < o.M;
+        if (N != o.N) return N < o.N;
+        if (K != o.K) return K < o.K;
+        if (dtype != o.dtype) return dtype < o.dtype;
+        if (a_major != o.a_major) return a_major < o.a_major;
+        if (b_major != o.b_major) return b_major < o.b_major;
+        if (c_major != o.c_major) return c_major < o.c_major;
+        return align < o.align;
+    }
+};
+std::mutex g_tune_mu;
+std::map<TuneKey, gemm_tuning> g_tune_table;
 
 struct DeviceState {
     std::once_flag once;
@@ -216,14 +247,14 @@ Problem normalise(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, i
 // two HBM passes over the operand, 48/n of the GEMM time for the other
 // dimension n, so it pays when n >= 512 and the product is large enough for
 // the extra launch not to matter.
-bool want_transpose(int64_t other_dim, const Problem& p) {
-    const int mode = g_simt_transpose.load();
+bool want_transpose(int64_t other_dim, const Problem& p, int mode) {
     if (mode == 1) return false;
     if (mode == 2) return true;
     return other_dim >= 512 && (double)p.M * (double)p.N * (double)p.K >= 2147483648.0;
 }
 
-int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_t s) {
+int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunConfig& cfg,
+              cudaStream_t s) {
     void* scratch[2] = {nullptr, nullptr};
     int rc = kOk;
     const void** ops[2] = {&p.A, &p.B};
@@ -232,7 +263,7 @@ int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_t
     const int64_t rows[2] = {p.M, p.N};
     const int64_t other[2] = {p.N, p.M};
     for (int i = 0; i < 2 && rc == kOk; ++i) {
-        if (!*kmaj[i] || !want_transpose(other[i], p)) continue;
+        if (!*kmaj[i] || !want_transpose(other[i], p, cfg.simt_transpose)) continue;
         const int64_t ld2 = round_up(rows[i], 4);  // 16-byte rows for vector copies
         if (cudaMallocFromPoolAsync(&scratch[i], (size_t)(p.K * ld2 * 4), pool, s) !=
             cudaSuccess) {
@@ -246,15 +277,16 @@ int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_t
         *lds[i] = ld2;
         *kmaj[i] = false;
     }
-    if (rc == kOk) rc = launch_sgemm_f32(p, dev, g_simt_config.load(), s);
+    if (rc == kOk) rc = launch_sgemm_f32(p, dev, cfg.simt_config, s);
     for (int i = 0; i < 2; ++i)
         if (scratch[i]) cudaFreeAsync(scratch[i], s);
     return rc;
 }
 
-int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_t s) {
+int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunConfig& cfg,
+               cudaStream_t s) {
     if (p.K == 0) return zero_fill(p.C, p.M, p.N, p.ldc, out_bytes(p.dtype), dev, s);
-    if (p.dtype == GEMM_F32) return run_sgemm(p, dev, pool, s);
+    if (p.dtype == GEMM_F32) return run_sgemm(p, dev, pool, cfg, s);
 
     // Tensor-core path: TMA needs 16-byte aligned bases and row pitches.
     void* scratch[2] = {nullptr, nullptr};
@@ -283,12 +315,45 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, cudaStream_
         *lds[i] = ld2;
     }
     if (rc == kOk)
-        rc = launch_gemm_tc(p, dev, g_cta_group.load(), g_wait_limit_ns.load(),
-                            g_fault_inject.load(), g_tc_store.load() != 1,
-                            g_tc_multicast.load() == 2, s);
+        rc = launch_gemm_tc(p, dev, cfg.cta_group, g_wait_limit_ns.load(),
+                            g_fault_inject.load(), cfg.tc_store != 1, cfg.multicast == 2, s);
     for (int i = 0; i < 2; ++i)
         if (scratch[i]) cudaFreeAsync(scratch[i], s);
     return rc;
+}
+
+bool aligned16_ld(const void* p, int64_t ld, int esize) {
+    return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ((ld * esize) & 15) == 0;
+}
+
+TuneKey make_key(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+                 const void* B, int64_t ldb, int b_major, const void* C, int64_t ldc,
+                 int c_major, int dtype) {
+    const int ie = in_bytes(dtype), oe = out_bytes(dtype);
+    const int align = (aligned16_ld(A, lda, ie) ? 1 : 0) | (aligned16_ld(B, ldb, ie) ? 2 : 0) |
+                      (aligned16_ld(C, ldc, oe) ? 4 : 0);
+    return TuneKey{M, N, K, dtype, a_major, b_major, c_major, align};
+}
+
+RunConfig resolve(const TuneKey& key) {
+    RunConfig c{g_simt_config.load(), g_simt_transpose.load(), g_cta_group.load(),
+                g_tc_multicast.load(), g_tc_store.load()};
+    gemm_tuning t{};
+    bool tuned = false;
+    {
+        std::lock_guard<std::mutex> lock(g_tune_mu);
+        auto it = g_tune_table.find(key);
+        if (it != g_tune_table.end()) {
+            t = it->second;
+            tuned = true;
+        }
+    }
+    if (c.simt_config == 0) c.simt_config = tuned && t.simt_config ? t.simt_config : 1;
+    if (c.simt_transpose == 0 && tuned) c.simt_transpose = t.simt_transpose;
+    if (c.cta_group == 0) c.cta_group = tuned && t.tc_cta_group ? t.tc_cta_group : 2;
+    if (c.multicast == 0) c.multicast = tuned && t.tc_multicast ? t.tc_multicast : 1;
+    if (c.tc_store == 0 && tuned) c.tc_store = t.tc_store;
+    return c;
 }
 
 }  // namespace
@@ -368,7 +433,9 @@ int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_majo
         if (rc != kOk) return rc;
         const Problem p =
             normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
-        return run_device(p, *dev, pool, static_cast<cudaStream_t>(stream));
+        const RunConfig cfg = resolve(
+            make_key(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype));
+        return run_device(p, *dev, pool, cfg, static_cast<cudaStream_t>(stream));
     } catch (...) {
         return kCuda;
     }
@@ -400,7 +467,9 @@ int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_m
                           epi->activation};
         cudaStream_t s = static_cast<cudaStream_t>(stream);
         if (K == 0) return launch_epilogue_only(p, *dev, s);
-        return run_device(p, *dev, pool, s);
+        const RunConfig cfg = resolve(
+            make_key(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype));
+        return run_device(p, *dev, pool, cfg, s);
     } catch (...) {
         return kCuda;
     }
@@ -455,7 +524,9 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         }
         const Problem p = normalise(M, N, K, dA, lda_d, a_major, dB, ldb_d, b_major, dC, ldc_d,
                                     c_major, dtype);
-        rc = run_device(p, *dev, pool, s);
+        const RunConfig cfg = resolve(make_key(M, N, K, dA, lda_d, a_major, dB, ldb_d, b_major,
+                                               dC, ldc_d, c_major, dtype));
+        rc = run_device(p, *dev, pool, cfg, s);
         if (rc == kOk &&
             cudaMemcpy2DAsync(C, ldc * oe, dC, ldc_d * oe, c_inner * oe, c_outer,
                               cudaMemcpyDeviceToHost, s) != cudaSuccess) {
@@ -467,6 +538,89 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
     } catch (...) {
         return kCuda;
     }
+}
+
+int gemm_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
+              const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
+              int dtype, int iterations, void* stream, gemm_tuning* out) {
+    try {
+        gemm_tuning best{};
+        if (out) *out = best;
+        int rc = validate(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+        if (rc != kOk) return rc;
+        if (M == 0 || N == 0 || K == 0) return kOk;
+        DeviceInfo* dev = nullptr;
+        cudaMemPool_t pool = nullptr;
+        rc = current_device(&dev, &pool);
+        if (rc != kOk) return rc;
+        if (iterations <= 0) iterations = 5;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        const Problem p =
+            normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
+
+        // candidate configurations for this problem
+        RunConfig cands[32];
+        int n = 0;
+        if (dtype == GEMM_F32) {
+            const bool any_kmajor = p.a_kmajor || p.b_kmajor;
+            for (int c = 1; c <= 6; ++c)
+                for (int t = 1; t <= (any_kmajor ? 2 : 1); ++t) cands[n++] = {c, t, 2, 1, 0};
+        } else {
+            const bool c_aligned = aligned16_ld(C, ldc, out_bytes(dtype));
+            const int modes[3][2] = {{1, 1}, {2, 1}, {2, 2}};
+            for (const auto& m : modes)
+                for (int st = c_aligned ? 0 : 1; st <= 1; ++st)
+                    cands[n++] = {1, 0, m[0], m[1], st};
+        }
+
+        cudaEvent_t e0 = nullptr, e1 = nullptr;
+        if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+            cudaGetLastError();
+            if (e0) cudaEventDestroy(e0);
+            return kCuda;
+        }
+        float best_ms = -1.f;
+        RunConfig best_cfg = cands[0];
+        for (int i = 0; i < n && rc == kOk; ++i) {
+            rc = run_device(p, *dev, pool, cands[i], s);  // warm-up
+            if (rc == kOk && cudaEventRecord(e0, s) != cudaSuccess) rc = kCuda;
+            for (int it = 0; it < iterations && rc == kOk; ++it)
+                rc = run_device(p, *dev, pool, cands[i], s);
+            float ms = 0.f;
+            if (rc == kOk && (cudaEventRecord(e1, s) != cudaSuccess ||
+                              cudaEventSynchronize(e1) != cudaSuccess ||
+                              cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess))
+                rc = kCuda;
+            if (rc != kOk) break;
+            ms /= (float)iterations;
+            if (best_ms < 0.f || ms < best_ms) {
+                best_ms = ms;
+                best_cfg = cands[i];
+            }
+        }
+        cudaEventDestroy(e0);
+        cudaEventDestroy(e1);
+        if (rc != kOk) {
+            cudaGetLastError();
+            return rc;
+        }
+        best = gemm_tuning{best_cfg.simt_config, best_cfg.simt_transpose, best_cfg.cta_group,
+                           best_cfg.multicast, best_cfg.tc_store, best_ms, n};
+        {
+            std::lock_guard<std::mutex> lock(g_tune_mu);
+            g_tune_table[make_key(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major,
+                                  dtype)] = best;
+        }
+        if (out) *out = best;
+        return kOk;
+    } catch (...) {
+        return kCuda;
+    }
+}
+
+void gemm_tune_reset(void) {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    g_tune_table.clear();
 }
 
 const char* gemm_strerror(int status) {

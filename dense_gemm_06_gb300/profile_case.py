@@ -47,6 +47,8 @@ def main(argv=None):
     ap.add_argument("--simt-config", type=int, default=0)
     ap.add_argument("--tc-store", type=int, default=0)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--tune", action="store_true",
+                    help="run gemm_tune first (records the fastest configuration)")
     a = ap.parse_args(argv)
     M, N, K, dtype, am, bm, dist, seed, lo, hi = CASES[a.case]
     if a.n:
@@ -71,6 +73,11 @@ def main(argv=None):
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_STORE, a.tc_store))
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
+    if a.tune:
+        rc, t = lg.gemm_tune(M, N, K, dA, lda, am, dB, ldb, bm, dC, N, 1, dtype, 5,
+                             s.cuda_stream)
+        lg.check(rc, "gemm_tune")
+        print(f"{a.case} {M}x{N}x{K} A{'KM'[am]} B{'KN'[bm]} tuned: {t}")
     for r in range(a.reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)

@@ -194,6 +194,41 @@ int gemm_noalloc(int64_t M, int64_t N, int64_t K,
                  void *C, int64_t ldc, int c_major,
                  int dtype, void *stream);
 
+/* A kernel configuration chosen by gemm_tune (the option values it stands
+   for; see enum gemm_option). */
+typedef struct gemm_tuning {
+    int simt_config;    /* fp32: FFMA tile configuration 1..6 */
+    int simt_transpose; /* fp32: 1 = run K-major operands as they are,
+                           2 = transpose them to MN-major first */
+    int tc_cta_group;   /* 16-bit: 1 or 2 CTAs per tile */
+    int tc_multicast;   /* 16-bit: 1 off, 2 B multicast across two pairs */
+    int tc_store;       /* 16-bit: 0 TMA store where possible, 1 st.global */
+    float ms;           /* measured time per call of the chosen configuration */
+    int candidates;     /* configurations measured */
+} gemm_tuning;
+
+/*
+ * gemm_tune -- per-problem configuration selection (the pages' autotune
+ * utilities, CuTe DSL `tune`/`autotune_jit`, done natively): runs every
+ * kernel configuration valid for this problem on the caller's buffers and
+ * stream (one warm-up call and `iterations` timed calls each, CUDA events),
+ * records the fastest in a process-wide table keyed by (M, N, K, dtype,
+ * majors, 16-byte alignment of A, B and C) and writes it to *out (may be
+ * NULL). Later gemm(), gemm_ex() and gemm_host() calls on a matching problem
+ * use the recorded configuration for every option left at 0 (automatic).
+ * C is overwritten with the product. Synchronises `stream`. iterations <= 0
+ * means 5. A problem with nothing to run (M, N or K zero) records nothing
+ * and returns GEMM_OK with out->candidates == 0. Status codes as gemm().
+ */
+int gemm_tune(int64_t M, int64_t N, int64_t K,
+              const void *A, int64_t lda, int a_major,
+              const void *B, int64_t ldb, int b_major,
+              void *C, int64_t ldc, int c_major,
+              int dtype, int iterations, void *stream, gemm_tuning *out);
+
+/* gemm_tune_reset -- forget every configuration gemm_tune recorded. */
+void gemm_tune_reset(void);
+
 /* gemm_strerror -- a static, NUL-terminated description of a status code. */
 const char *gemm_strerror(int status);
 
