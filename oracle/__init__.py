@@ -66,6 +66,8 @@ def _load():
             lib.oracle_f32_to_f64.restype = ctypes.c_double
             lib.oracle_f32_to_f64.argtypes = [ctypes.c_uint32]
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_softmax_rows.restype = ctypes.c_int
+            lib.oracle_softmax_rows.argtypes = [i64, i64, p, i64, p, i64]
             lib.oracle_epilogue.restype = ctypes.c_int
             lib.oracle_epilogue.argtypes = [i64, i64, p, p, i64, p, i64, ctypes.c_double,
                                             ctypes.c_double, p, i64, ctypes.c_int, ctypes.c_int,
@@ -152,3 +154,16 @@ def epilogue_ref(M: int, N: int, C_ref: np.ndarray, alpha: float, beta: float,
     if rc != 0:
         raise ValueError(f"oracle_epilogue rejected the arguments (status {rc})")
     return D
+
+
+def softmax_ref(M: int, N: int, x: np.ndarray, ldx: int) -> np.ndarray:
+    """Row softmax of an fp32 M x N matrix (row pitch ldx) in fp64 (M x N)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.zeros((M, N), dtype=np.float64)
+    if M == 0 or N == 0:
+        return y
+    rc = lib.oracle_softmax_rows(M, N, x.ctypes.data, ldx, y.ctypes.data, N)
+    if rc != 0:
+        raise ValueError(f"oracle_softmax_rows rejected the arguments (status {rc})")
+    return y

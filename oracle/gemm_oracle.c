@@ -283,3 +283,38 @@ int oracle_epilogue(int64_t M, int64_t N, const double *C_ref,
     }
     return ORACLE_OK;
 }
+
+/*
+ * oracle_softmax_rows: y[m][n] = exp(x[m][n] - mx) / sum_j exp(x[m][j] - mx),
+ * mx = max_j x[m][j], per row, in fp64 (x and y fp32 storage, row pitches
+ * ldx/ldy in elements). The numerically stable row softmax of the Gluon
+ * Multi-CTA tutorial's multi-CTA softmax kernel: row max, exponentials of the
+ * shifted row, their sum, one division. Rows are independent; each is one
+ * sequential max, one sequential sum.
+ */
+int oracle_softmax_rows(int64_t M, int64_t N, const float *x, int64_t ldx, double *y,
+                        int64_t ldy) {
+    if (M < 0 || N < 0) return ORACLE_EINVAL;
+    if (M == 0 || N == 0) return ORACLE_OK;
+    if (!x || !y || ldx < N || ldy < N) return ORACLE_EINVAL;
+    for (int64_t m = 0; m < M; ++m) {
+        const float *xr = x + m * ldx;
+        double *yr = y + m * ldy;
+        double mx = -INFINITY;
+        for (int64_t n = 0; n < N; ++n) {
+            uint32_t u;
+            memcpy(&u, xr + n, 4);
+            double v = oracle_f32_to_f64(u);
+            if (v > mx) mx = v;
+        }
+        double sum = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            uint32_t u;
+            memcpy(&u, xr + n, 4);
+            yr[n] = exp(oracle_f32_to_f64(u) - mx);
+            sum += yr[n];
+        }
+        for (int64_t n = 0; n < N; ++n) yr[n] /= sum;
+    }
+    return ORACLE_OK;
+}

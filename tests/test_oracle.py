@@ -375,3 +375,40 @@ def test_epilogue_rejects_bad_arguments():
         oracle.epilogue_ref(2, 2, C, 1.0, 0.5)              # beta != 0 without C_in
     with pytest.raises(ValueError):
         oracle.epilogue_ref(2, 2, C, 1.0, 0.0, rows=[2])    # row out of range
+
+
+# ------------------------------------------------------------ row softmax --
+# The Gluon Multi-CTA tutorial's multi-CTA softmax: y = exp(x - max) / sum.
+
+def test_softmax_pins():
+    import math
+    # hand-worked: x = [0, ln 2, ln 5] -> [1, 2, 5] / 8
+    x = np.array([0.0, math.log(2.0), math.log(5.0)], np.float32)
+    y = oracle.softmax_ref(1, 3, x, 3)[0]
+    xd = x.astype(np.float64)
+    want = np.exp(xd - xd.max()) / np.exp(xd - xd.max()).sum()
+    assert np.allclose(y, want, rtol=1e-15, atol=0)
+    assert abs(y[0] - 1 / 8) < 1e-7 and abs(y[2] - 5 / 8) < 1e-7
+    # uniform rows give 1/N; rows sum to one; shift invariance; padding ignored
+    rng = np.random.default_rng(4)
+    M, N, ld = 6, 37, 40
+    xs = np.full(M * ld, np.nan, np.float32)
+    body = (rng.integers(-64, 64, (M, N)) / 8.0).astype(np.float32)  # exact under +16
+    xs.reshape(M, ld)[:, :N] = body
+    y = oracle.softmax_ref(M, N, xs, ld)
+    assert np.allclose(y.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    shifted = xs.copy()
+    shifted.reshape(M, ld)[:, :N] += 16.0
+    assert np.array_equal(shifted.reshape(M, ld)[:, :N] - 16.0, body)
+    assert np.allclose(oracle.softmax_ref(M, N, shifted, ld), y, rtol=1e-13, atol=0)
+    assert np.allclose(oracle.softmax_ref(2, 9, np.full(18, 1.5, np.float32), 9), 1 / 9,
+                       rtol=1e-15, atol=0)
+    # monotone in x, and the largest input gets the largest output
+    assert all(np.argmax(y[i]) == np.argmax(body[i]) for i in range(M))
+    order = np.argsort(body[0])
+    assert np.all(np.diff(y[0][order]) >= 0)
+    # a dominant entry takes (almost) all the mass
+    xd = np.zeros(50, np.float32)
+    xd[7] = 60.0
+    yd = oracle.softmax_ref(1, 50, xd, 50)[0]
+    assert abs(yd[7] - 1.0) < 1e-24 and yd[0] == np.exp(-60.0) * yd[7]
