@@ -55,7 +55,7 @@ OUT_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f32", GEMM_BF16_F32: "f32",
             GEMM_F16_F16: "f16", GEMM_BF16_BF16: "bf16"}
 
 EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_noalloc", "gemm_tune", "gemm_tune_reset",
-           "gemm_strerror", "gemm_check_device_error", "gemm_release_workspace",
+           "softmax_rows", "gemm_strerror", "gemm_check_device_error", "gemm_release_workspace",
            "gemm_launch_count", "gemm_set_option", "gemm_get_option")
 
 _lock = threading.Lock()
@@ -89,6 +89,8 @@ def load(path: str = LIB_PATH):
         lib.gemm_tune.restype = ci
         lib.gemm_tune.argtypes = sig[:-1] + [ci, vp, ctypes.POINTER(GemmTuning)]
         lib.gemm_tune_reset.restype, lib.gemm_tune_reset.argtypes = None, []
+        lib.softmax_rows.restype = ci
+        lib.softmax_rows.argtypes = [i64, i64, vp, i64, vp, i64, vp]
         lib.gemm_strerror.restype, lib.gemm_strerror.argtypes = ctypes.c_char_p, [ci]
         lib.gemm_check_device_error.restype = ci
         lib.gemm_check_device_error.argtypes = [vp]
@@ -167,6 +169,11 @@ def gemm_tune(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype,
 
 def gemm_tune_reset() -> None:
     load().gemm_tune_reset()
+
+
+def softmax_rows(M, N, x, ldx, y, ldy, stream=None) -> int:
+    """Row softmax of an fp32 matrix over thread-block clusters; see gemm.h."""
+    return load().softmax_rows(M, N, _ptr(x), ldx, _ptr(y), ldy, _stream(stream))
 
 
 def gemm_strerror(status: int) -> str:

@@ -623,6 +623,25 @@ void gemm_tune_reset(void) {
     g_tune_table.clear();
 }
 
+int softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float* y, int64_t ldy,
+                 void* stream) {
+    try {
+        if (M < 0 || N < 0 || M > INT32_MAX || N > INT32_MAX) return kInvalidArg;
+        if (M == 0 || N == 0) return kOk;
+        if (!x || !y || ldx < N || ldy < N) return kInvalidArg;
+        if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(y) % 4)
+            return kInvalidArg;
+        if (!span_ok(M, N, ldx, 4) || !span_ok(M, N, ldy, 4)) return kInvalidArg;
+        if (N > softmax_max_cols()) return kUnsupported;
+        DeviceInfo* dev = nullptr;
+        const int rc = current_device(&dev, nullptr);
+        if (rc != kOk) return rc;
+        return launch_softmax_rows(M, N, x, ldx, y, ldy, static_cast<cudaStream_t>(stream));
+    } catch (...) {
+        return kCuda;
+    }
+}
+
 const char* gemm_strerror(int status) {
     switch (status) {
         case GEMM_OK: return "success";

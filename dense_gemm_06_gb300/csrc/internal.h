@@ -67,6 +67,12 @@ Problem normalised(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
                    int dtype);
 int error_word_address(unsigned int** out);
 
+// Row softmax over thread-block clusters (softmax_cluster.cu); rows longer
+// than softmax_max_cols() are not supported.
+int64_t softmax_max_cols();
+int launch_softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float* y, int64_t ldy,
+                        cudaStream_t stream);
+
 // C = act(beta * C + bias) in place (the K == 0 case of gemm_ex), rows x cols
 // of the normalised row-major C.
 int launch_epilogue_only(const Problem& p, const DeviceInfo& dev, cudaStream_t stream);

@@ -1,0 +1,62 @@
+"""Row-softmax bandwidth on the Gluon Multi-CTA tutorial's benchmark shapes.
+
+    python -m dense_gemm_06_gb300.softmax_bench [--reps 20]
+
+For each shape (M rows of N fp32 values) prints the CTAs per row, the time per
+call (CUDA events, median of `reps` back-to-back calls after warm-up) and the
+bandwidth counted as the tutorial counts it: 2 * M * N * 4 bytes (one read
+of x, one write of y) per call. Inputs are seeded U[-1, 1) values.
+"""
+
+from __future__ import annotations
+
+import argparse
+import os
+import statistics
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+SHAPES = [(2 ** 15, 2 ** 8), (2 ** 15, 2 ** 9), (2 ** 15, 2 ** 10), (2 ** 15, 2 ** 11),
+          (2 ** 15, 2 ** 12), (2 ** 15, 2 ** 13), (2 ** 15, 2 ** 14), (2 ** 15, 2 ** 15),
+          (2 ** 15, 2 ** 16), (2 ** 14, 2 ** 17), (2 ** 13, 2 ** 18)]
+
+
+def main(argv=None):
+    import torch
+
+    import datagen
+    import dense_gemm_06_gb300 as lg
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--reps", type=int, default=20)
+    a = ap.parse_args(argv)
+    lg.load()
+    torch.cuda.set_device(0)
+    s = torch.cuda.Stream()
+    print("   shape           CTAs/row  time (ms)  bandwidth (GB/s)")
+    for M, N in SHAPES:
+        x = torch.from_numpy(datagen.logical(M, N, dtype="f32", dist="pm1", seed=M ^ N)).cuda()
+        y = torch.empty_like(x)
+        cs = 1
+        while cs * 32768 < N:
+            cs *= 2
+        for _ in range(3):
+            lg.check(lg.softmax_rows(M, N, x, N, y, N, s.cuda_stream))
+        times = []
+        for _ in range(a.reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            lg.check(lg.softmax_rows(M, N, x, N, y, N, s.cuda_stream))
+            e1.record(s)
+            s.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        print(f"{M:>7} x {N:<7} {cs:>6}  {ms:>9.3f}  {2 * M * N * 4 / (ms * 1e-3) / 1e9:>16.1f}")
+        del x, y
+
+
+if __name__ == "__main__":
+    main()

@@ -229,6 +229,22 @@ int gemm_tune(int64_t M, int64_t N, int64_t K,
 /* gemm_tune_reset -- forget every configuration gemm_tune recorded. */
 void gemm_tune_reset(void);
 
+/*
+ * softmax_rows -- y[m][n] = exp(x[m][n] - max_j x[m][j]) / sum_j exp(x[m][j] -
+ * max_j x[m][j]) for every row m < M of an fp32 matrix (row pitches ldx and
+ * ldy in elements, >= N; 4-byte aligned device pointers). The multi-CTA row
+ * softmax of the Gluon Multi-CTA tutorial: rows up to 1024 columns take
+ * one warp each, rows up to 32768 one CTA, longer rows a thread-block
+ * cluster of up to 16 CTAs (one per 32768 columns); every thread keeps its
+ * values in registers and the CTAs of a cluster combine their partial
+ * maximum and sum through distributed shared memory, so x is read once and
+ * y written once. N up to 524288; longer rows return GEMM_ERR_UNSUPPORTED.
+ * y may be x itself (ldy == ldx); other overlaps are undefined.
+ * Asynchronous on `stream`; status codes as gemm().
+ */
+int softmax_rows(int64_t M, int64_t N, const float *x, int64_t ldx, float *y, int64_t ldy,
+                 void *stream);
+
 /* gemm_strerror -- a static, NUL-terminated description of a status code. */
 const char *gemm_strerror(int status);
 

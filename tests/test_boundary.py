@@ -94,6 +94,15 @@ def test_gemm_ex_host_checks(lib):
     assert lg.gemm_ex(0, 4, 4, P, 4, 0, P, 4, 0, P, 4, 1, lg.GEMM_F32, beta=1.0) == lg.GEMM_OK
 
 
+def test_softmax_host_checks(lib):
+    assert lg.softmax_rows(-1, 4, P, 4, P, 4) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.softmax_rows(4, 4, 0, 4, P, 4) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.softmax_rows(4, 4, P, 3, P, 4) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.softmax_rows(4, 4, P + 2, 4, P, 4) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.softmax_rows(0, 4, 0, 4, 0, 4) == lg.GEMM_OK
+    assert lg.softmax_rows(2, 524289, P, 524289, P, 524289) == lg.GEMM_ERR_UNSUPPORTED
+
+
 def test_degenerate_sizes_need_no_device(lib):
     assert call(M=0) == lg.GEMM_OK
     assert call(N=0, C=0) == lg.GEMM_OK          # nothing addressed: C may be NULL
