@@ -636,7 +636,8 @@ int softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float* y, in
         DeviceInfo* dev = nullptr;
         const int rc = current_device(&dev, nullptr);
         if (rc != kOk) return rc;
-        return launch_softmax_rows(M, N, x, ldx, y, ldy, static_cast<cudaStream_t>(stream));
+        return launch_softmax_rows(M, N, x, ldx, y, ldy, *dev, g_wait_limit_ns.load(),
+                                   static_cast<cudaStream_t>(stream));
     } catch (...) {
         return kCuda;
     }

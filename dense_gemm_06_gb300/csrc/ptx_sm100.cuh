@@ -134,6 +134,25 @@ __device__ __forceinline__ void tma_load_2d_mc_pair(uint32_t dst, const void* ma
         :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "h"(mask) : "memory");
 }
 
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`
+// (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// Stores (a, b) at `addr` in a cluster peer's shared memory and completes 8
+// transaction bytes on the peer's mbarrier `remote_bar` (both addresses from
+// mapa, 8-byte aligned).
+__device__ __forceinline__ void st_async_v2_f32(uint32_t addr, float a, float b,
+                                                uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+        :: "r"(addr), "f"(a), "f"(b), "r"(remote_bar) : "memory");
+}
+
 // 2-D tiled TMA store from this CTA's shared memory (bulk async-group).
 __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"

@@ -24,6 +24,23 @@ SHAPES = [(2 ** 15, 2 ** 8), (2 ** 15, 2 ** 9), (2 ** 15, 2 ** 10), (2 ** 15, 2 
           (2 ** 15, 2 ** 16), (2 ** 14, 2 ** 17), (2 ** 13, 2 ** 18)]
 
 
+def ctas_per_row(N: int) -> int:
+    """CTAs per row as softmax_rows lays rows out (16-byte-aligned rows): one
+    CTA up to 32768 columns, then clusters of 8192-column CTAs, then of
+    16384-column CTAs once 16 of 8192 no longer cover a row."""
+    if N <= 32768:
+        return 1
+    cs = 1
+    while cs * 8192 < N:
+        cs *= 2
+    if cs <= 16:
+        return cs
+    cs = 1
+    while cs * 16384 < N:
+        cs *= 2
+    return cs
+
+
 def main(argv=None):
     import torch
 
@@ -40,9 +57,7 @@ def main(argv=None):
     for M, N in SHAPES:
         x = torch.from_numpy(datagen.logical(M, N, dtype="f32", dist="pm1", seed=M ^ N)).cuda()
         y = torch.empty_like(x)
-        cs = 1
-        while cs * 32768 < N:
-            cs *= 2
+        cs = ctas_per_row(N)
         for _ in range(3):
             lg.check(lg.softmax_rows(M, N, x, N, y, N, s.cuda_stream))
         times = []

@@ -1,7 +1,8 @@
 """GPU parity of softmax_rows (the Gluon Multi-CTA tutorial's multi-CTA row
 softmax) against the fp64 oracle: the tutorial's test shapes (64 x 64,
 64 x 256, 16 x 65536), every cluster size (1, 2, 4, 8, 16 CTAs per row),
-ragged and misaligned rows, in-place use and large-magnitude rows.
+ragged and misaligned rows, in-place use, large-magnitude rows and long
+rows with many more rows than resident clusters.
 Acceptance: |y - y_ref| <= 1e-5 * y_ref + 1e-30 per element (fp32 exp and a
 tree sum of at most 2^18 terms stay well inside 1e-5 relative; the absolute
 term only covers results that underflow fp32)."""
@@ -81,3 +82,11 @@ def test_large_magnitudes_are_stable():
     y = run_softmax(6, 70000, scale=40.0, seed=6)    # |x| up to ~200: exp would overflow unshifted
     assert np.allclose(y.sum(axis=1), 1.0, rtol=0, atol=1e-5)
     run_softmax(6, 3000, dist="pm1", scale=1e-3, seed=7)  # nearly uniform rows
+
+
+@pytest.mark.parametrize("M,N,ld_pad", [(1000, 40000, 0), (300, 65540, 4), (64, 262144, 0),
+                                        (200, 131073, 3), (152, 98304, 0)])
+def test_long_rows_many_per_cluster(M, N, ld_pad):
+    # more rows than resident clusters: each cluster walks several rows and
+    # prefetches the next one while reducing the current one
+    run_softmax(M, N, ld_pad=ld_pad, seed=(M + N) % 89)
