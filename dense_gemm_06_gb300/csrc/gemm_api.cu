@@ -32,6 +32,7 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_cta_group{0};
 std::atomic<int> g_fault_inject{0};
+std::atomic<int> g_softmax_fault_inject{0};
 std::atomic<int> g_simt_config{0};
 std::atomic<int> g_simt_transpose{0};
 std::atomic<int> g_tc_store{0};
@@ -637,6 +638,7 @@ int softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float* y, in
         const int rc = current_device(&dev, nullptr);
         if (rc != kOk) return rc;
         return launch_softmax_rows(M, N, x, ldx, y, ldy, *dev, g_wait_limit_ns.load(),
+                                   g_softmax_fault_inject.load(),
                                    static_cast<cudaStream_t>(stream));
     } catch (...) {
         return kCuda;
@@ -726,6 +728,10 @@ int gemm_set_option(int option, int64_t value) {
             if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             g_tc_multicast.store((int)value);
             return GEMM_OK;
+        case GEMM_OPT_SOFTMAX_FAULT_INJECT:
+            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            g_softmax_fault_inject.store((int)value);
+            return GEMM_OK;
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -739,6 +745,7 @@ int64_t gemm_get_option(int option) {
         case GEMM_OPT_SIMT_TRANSPOSE: return g_simt_transpose.load();
         case GEMM_OPT_TC_STORE: return g_tc_store.load();
         case GEMM_OPT_TC_MULTICAST: return g_tc_multicast.load();
+        case GEMM_OPT_SOFTMAX_FAULT_INJECT: return g_softmax_fault_inject.load();
         default: return -1;
     }
 }

@@ -71,7 +71,8 @@ int error_word_address(unsigned int** out);
 // than softmax_max_cols() are not supported.
 int64_t softmax_max_cols();
 int launch_softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float* y, int64_t ldy,
-                        const DeviceInfo& dev, uint64_t wait_limit_ns, cudaStream_t stream);
+                        const DeviceInfo& dev, uint64_t wait_limit_ns, int fault_inject,
+                        cudaStream_t stream);
 
 // C = act(beta * C + bias) in place (the K == 0 case of gemm_ex), rows x cols
 // of the normalised row-major C.

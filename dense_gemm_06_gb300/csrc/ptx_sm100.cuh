@@ -59,6 +59,16 @@ __device__ __forceinline__ void cluster_sync_all() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split cluster barrier: arrive without ordering memory (the mbarrier-init
+// fence provides what peers need), then wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // --------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -132,15 +142,6 @@ __device__ __forceinline__ void tma_load_2d_mc_pair(uint32_t dst, const void* ma
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;"
         :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "h"(mask) : "memory");
-}
-
-// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`
-// (both addresses 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
-                                             uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
 // Stores (a, b) at `addr` in a cluster peer's shared memory and completes 8

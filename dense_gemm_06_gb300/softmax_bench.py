@@ -1,11 +1,13 @@
 """Row-softmax bandwidth on the Gluon Multi-CTA tutorial's benchmark shapes.
 
-    python -m dense_gemm_06_gb300.softmax_bench [--reps 20]
+    python -m dense_gemm_06_gb300.softmax_bench [--reps 20] [--no-graph]
 
 For each shape (M rows of N fp32 values) prints the CTAs per row, the time per
-call (CUDA events, median of `reps` back-to-back calls after warm-up) and the
-bandwidth counted as the tutorial counts it: 2 * M * N * 4 bytes (one read
-of x, one write of y) per call. Inputs are seeded U[-1, 1) values.
+call and the bandwidth counted as the tutorial counts it: 2 * M * N * 4 bytes
+(one read of x, one write of y) per call. Like the tutorial's benchmark, the
+time is taken over a CUDA graph of 10 back-to-back calls (CUDA events around
+each replay, median of `reps` replays, after warm-up); --no-graph times
+single calls instead. Inputs are seeded U[-1, 1) values.
 """
 
 from __future__ import annotations
@@ -24,17 +26,12 @@ SHAPES = [(2 ** 15, 2 ** 8), (2 ** 15, 2 ** 9), (2 ** 15, 2 ** 10), (2 ** 15, 2 
           (2 ** 15, 2 ** 16), (2 ** 14, 2 ** 17), (2 ** 13, 2 ** 18)]
 
 
+GRAPH_CALLS = 10
+
+
 def ctas_per_row(N: int) -> int:
-    """CTAs per row as softmax_rows lays rows out (16-byte-aligned rows): one
-    CTA up to 32768 columns, then clusters of 8192-column CTAs, then of
-    16384-column CTAs once 16 of 8192 no longer cover a row."""
-    if N <= 32768:
-        return 1
-    cs = 1
-    while cs * 8192 < N:
-        cs *= 2
-    if cs <= 16:
-        return cs
+    """CTAs per row as softmax_rows lays out 16-byte-aligned rows: one CTA up
+    to 16384 columns, then a cluster of 16384-column CTAs."""
     cs = 1
     while cs * 16384 < N:
         cs *= 2
@@ -49,6 +46,8 @@ def main(argv=None):
 
     ap = argparse.ArgumentParser()
     ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time single calls instead of a CUDA graph of back-to-back calls")
     a = ap.parse_args(argv)
     lg.load()
     torch.cuda.set_device(0)
@@ -60,14 +59,35 @@ def main(argv=None):
         cs = ctas_per_row(N)
         for _ in range(3):
             lg.check(lg.softmax_rows(M, N, x, N, y, N, s.cuda_stream))
+        s.synchronize()
         times = []
-        for _ in range(a.reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(s)
-            lg.check(lg.softmax_rows(M, N, x, N, y, N, s.cuda_stream))
-            e1.record(s)
-            s.synchronize()
-            times.append(e0.elapsed_time(e1))
+        if a.graph:
+            # the tutorial's method: back-to-back calls replayed from a CUDA
+            # graph, so host launch gaps do not count
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(GRAPH_CALLS):
+                    lg.check(lg.softmax_rows(M, N, x, N, y, N, s.cuda_stream))
+            with torch.cuda.stream(s):  # replay() launches on the current stream
+                g.replay()
+                s.synchronize()
+                for _ in range(a.reps):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(s)
+                    g.replay()
+                    e1.record(s)
+                    s.synchronize()
+                    times.append(e0.elapsed_time(e1) / GRAPH_CALLS)
+            del g
+        else:
+            for _ in range(a.reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                lg.check(lg.softmax_rows(M, N, x, N, y, N, s.cuda_stream))
+                e1.record(s)
+                s.synchronize()
+                times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
         print(f"{M:>7} x {N:<7} {cs:>6}  {ms:>9.3f}  {2 * M * N * 4 / (ms * 1e-3) / 1e9:>16.1f}")
         del x, y

@@ -233,14 +233,17 @@ void gemm_tune_reset(void);
  * softmax_rows -- y[m][n] = exp(x[m][n] - max_j x[m][j]) / sum_j exp(x[m][j] -
  * max_j x[m][j]) for every row m < M of an fp32 matrix (row pitches ldx and
  * ldy in elements, >= N; 4-byte aligned device pointers). The multi-CTA row
- * softmax of the Gluon Multi-CTA tutorial: rows up to 1024 columns take
- * one warp each, rows up to 32768 one CTA, longer rows a thread-block
- * cluster of up to 16 CTAs (one per 32768 columns); every thread keeps its
- * values in registers and the CTAs of a cluster combine their partial
- * maximum and sum through distributed shared memory, so x is read once and
- * y written once. N up to 524288; longer rows return GEMM_ERR_UNSUPPORTED.
- * y may be x itself (ldy == ldx); other overlaps are undefined.
- * Asynchronous on `stream`; status codes as gemm().
+ * softmax of the Gluon Multi-CTA tutorial: rows up to 1024 columns take one
+ * warp each, rows up to 16384 one CTA, longer rows a thread-block cluster of
+ * up to 16 CTAs that combine their partial maxima and sums through
+ * distributed shared memory, so x is read once and y written once. A
+ * cluster's CTAs take 16384 columns each for aligned rows (x and y 16-byte
+ * aligned, ldx and ldy multiples of 4, N <= 262144), else 32768. N up to
+ * 524288; longer rows return GEMM_ERR_UNSUPPORTED. y may be x itself (ldy == ldx); other overlaps are
+ * undefined. Asynchronous on `stream`; status codes as gemm(). The aligned
+ * cluster layout's wait for its peers' partials is bounded by
+ * GEMM_OPT_WAIT_LIMIT_NS; one that runs out is reported by
+ * gemm_check_device_error() as GEMM_ERR_TIMEOUT.
  */
 int softmax_rows(int64_t M, int64_t N, const float *x, int64_t ldx, float *y, int64_t ldy,
                  void *stream);
@@ -309,7 +312,13 @@ enum gemm_option {
        (currently off), 1 = off, 2 = on: clusters of two CTA pairs compute
        vertically adjacent 256 x 256 tiles and each half of the shared B tile
        is loaded once per cluster and multicast by TMA to both pairs. */
-    GEMM_OPT_TC_MULTICAST = 7
+    GEMM_OPT_TC_MULTICAST = 7,
+    /* Test hook for softmax_rows' timeout path: 1 makes the first CTA of the
+       first row's cluster (aligned rows of 16385..262144 columns) withhold
+       its partial, so that row's CTAs wait out GEMM_OPT_WAIT_LIMIT_NS and
+       report GEMM_ERR_TIMEOUT through gemm_check_device_error; the row's y
+       is then undefined. 0 (default) = off. */
+    GEMM_OPT_SOFTMAX_FAULT_INJECT = 8
 };
 
 /* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */

@@ -4,11 +4,16 @@ the epilogue waits on a barrier that nothing completes; the wait must run
 out after GEMM_OPT_WAIT_LIMIT_NS, the kernel must wind down (the MMA and
 producer roles see the error word and stop, in-flight work drains, TMEM is
 released), gemm_check_device_error must report GEMM_ERR_TIMEOUT once, and the
-device must stay usable for correct GEMMs afterwards."""
+device must stay usable for correct GEMMs afterwards. The same holds for
+softmax_rows' cluster exchange (GEMM_OPT_SOFTMAX_FAULT_INJECT: one CTA
+withholds its partial, so its row's CTAs wait out the limit)."""
 
+import numpy as np
 import pytest
 
+import datagen
 import dense_gemm_06_gb300 as lg
+import oracle
 from gpu_util import check_full, make_operands, run_device_gemm
 
 pytestmark = pytest.mark.gpu
@@ -50,3 +55,29 @@ def test_stalled_wait_times_out_and_device_recovers(cta_group):
         C = run_device_gemm(300, 520, 200, dtype, A, lda, 0, B, ldb, 1, cta_group=cta_group)
         check_full(C, 300, 520, 200, dtype, A, lda, 0, B, ldb, 1, exact=True,
                    what=f"after timeout (cg={cta_group})")
+
+
+def test_withheld_softmax_partial_times_out_and_device_recovers():
+    import torch
+    M, N = 6, 65536  # aligned rows of 65536 columns: clusters of 4 CTAs
+    x = datagen.logical(M, N, dtype="f32", dist="normal", seed=11).astype(np.float32)
+    dx = torch.from_numpy(x).cuda()
+    dy = torch.empty_like(dx)
+    assert lg.gemm_check_device_error() == lg.GEMM_OK
+    saved = {o: lg.gemm_get_option(o) for o in (lg.GEMM_OPT_WAIT_LIMIT_NS,
+                                                lg.GEMM_OPT_SOFTMAX_FAULT_INJECT)}
+    try:
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_WAIT_LIMIT_NS, 20_000_000))
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_SOFTMAX_FAULT_INJECT, 1))
+        assert lg.softmax_rows(M, N, dx, N, dy, N) == lg.GEMM_OK
+        assert lg.gemm_check_device_error() == lg.GEMM_ERR_TIMEOUT
+        assert lg.gemm_check_device_error() == lg.GEMM_OK
+    finally:
+        for o, v in saved.items():
+            lg.gemm_set_option(o, v)
+    # the context is intact and the exchange works again
+    lg.check(lg.softmax_rows(M, N, dx, N, dy, N), "softmax_rows")
+    lg.check(lg.gemm_check_device_error(), "device error word")
+    y = dy.cpu().numpy().astype(np.float64)
+    y_ref = oracle.softmax_ref(M, N, x.ravel(), N)
+    assert np.all(np.abs(y - y_ref) <= 1e-5 * y_ref + 1e-30)
