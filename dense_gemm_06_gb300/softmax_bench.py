@@ -1,6 +1,6 @@
 """Row-softmax bandwidth on the Gluon Multi-CTA tutorial's benchmark shapes.
 
-    python -m dense_gemm_06_gb300.softmax_bench [--reps 20] [--no-graph]
+    python -m dense_gemm_06_gb300.softmax_bench [--reps 20] [--no-graph] [--shape M N]
 
 For each shape (M rows of N fp32 values) prints the CTAs per row, the time per
 call and the bandwidth counted as the tutorial counts it: 2 * M * N * 4 bytes
@@ -48,12 +48,14 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time single calls instead of a CUDA graph of back-to-back calls")
+    ap.add_argument("--shape", type=int, nargs=2, metavar=("M", "N"),
+                    help="run this one shape instead of the tutorial's list")
     a = ap.parse_args(argv)
     lg.load()
     torch.cuda.set_device(0)
     s = torch.cuda.Stream()
     print("   shape           CTAs/row  time (ms)  bandwidth (GB/s)")
-    for M, N in SHAPES:
+    for M, N in ([tuple(a.shape)] if a.shape else SHAPES):
         x = torch.from_numpy(datagen.logical(M, N, dtype="f32", dist="pm1", seed=M ^ N)).cuda()
         y = torch.empty_like(x)
         cs = ctas_per_row(N)
