@@ -324,17 +324,19 @@ def test_pins_catch_planted_mistakes(kind):
 # D = act(alpha * C + beta * C_in + bias): the CuTe Ampere SGEMM example's
 # epilogue_op hook with scaling, bias and activation written out.
 
-def test_epilogue_pins():
+def epilogue_pins(epi):
+    """Every epilogue pin, against the callable `epi` (the oracle's signature);
+    raises AssertionError on the first that fails."""
     rng = np.random.default_rng(3)
     M, N = 5, 7
     C = rng.integers(-50, 50, (M, N)).astype(np.float64)
     # identity
-    assert np.array_equal(oracle.epilogue_ref(M, N, C, 1.0, 0.0), C)
+    assert np.array_equal(epi(M, N, C, 1.0, 0.0), C)
     # scaling only
-    assert np.array_equal(oracle.epilogue_ref(M, N, C, -0.5, 0.0), -0.5 * C)
+    assert np.array_equal(epi(M, N, C, -0.5, 0.0), -0.5 * C)
     # bias broadcast along rows, indexed by the column
     bias = np.arange(N, dtype=np.float32) * 3 - 4
-    D = oracle.epilogue_ref(M, N, C, 1.0, 0.0, bias=bias)
+    D = epi(M, N, C, 1.0, 0.0, bias=bias)
     assert np.array_equal(D - C, np.broadcast_to(bias.astype(np.float64), (M, N)))
     # beta * C_in in both layouts of C (and 16-bit storage), dyadic => exact
     Lc = rng.integers(-8, 8, (M, N)).astype(np.float64)
@@ -342,19 +344,19 @@ def test_epilogue_pins():
     row_major[:, :N] = Lc
     col_major = np.full(N * (M + 1), np.nan, np.float32).reshape(N, M + 1)
     col_major[:, :M] = Lc.T
-    D1 = oracle.epilogue_ref(M, N, C, 1.0, 0.25, C_in=row_major.ravel(), ldc=N + 2, c_major=1)
-    D0 = oracle.epilogue_ref(M, N, C, 1.0, 0.25, C_in=col_major.ravel(), ldc=M + 1, c_major=0)
+    D1 = epi(M, N, C, 1.0, 0.25, C_in=row_major.ravel(), ldc=N + 2, c_major=1)
+    D0 = epi(M, N, C, 1.0, 0.25, C_in=col_major.ravel(), ldc=M + 1, c_major=0)
     assert np.array_equal(D1, C + 0.25 * Lc) and np.array_equal(D0, D1)
     bf = datagen.to_storage(Lc.ravel(), "bf16")
-    D2 = oracle.epilogue_ref(M, N, C, 1.0, 0.25, C_in=bf, ldc=N, c_major=1, c_dtype="bf16")
+    D2 = epi(M, N, C, 1.0, 0.25, C_in=bf, ldc=N, c_major=1, c_dtype="bf16")
     assert np.array_equal(D2, D1)
     # beta == 0 never reads C_in (NaN storage must not leak in)
     nan_c = np.full(M * N, np.nan, np.float32)
-    assert np.array_equal(oracle.epilogue_ref(M, N, C, 1.0, 0.0, C_in=nan_c, ldc=N), C)
+    assert np.array_equal(epi(M, N, C, 1.0, 0.0, C_in=nan_c, ldc=N), C)
     # ReLU
-    assert np.array_equal(oracle.epilogue_ref(M, N, C, 1.0, 0.0, act="relu"), np.maximum(C, 0))
+    assert np.array_equal(epi(M, N, C, 1.0, 0.0, act="relu"), np.maximum(C, 0))
     # GELU: x * Phi(x); Phi(1) = 0.8413447460685429 (normal table), odd part = x
-    g = oracle.epilogue_ref(1, 5, np.array([[1.0, -1.0, 0.0, 10.0, -10.0]]), 1.0, 0.0,
+    g = epi(1, 5, np.array([[1.0, -1.0, 0.0, 10.0, -10.0]]), 1.0, 0.0,
                             act="gelu")[0]
     assert abs(g[0] - 0.8413447460685429) < 1e-15
     assert abs(g[1] + (1 - 0.8413447460685429)) < 1e-15
@@ -362,11 +364,15 @@ def test_epilogue_pins():
     assert abs((g[0] - g[1]) - 1.0) < 1e-15
     # sampled block equals the same block of the full result
     rows, cols = np.array([4, 0]), np.array([6, 2, 3])
-    Db = oracle.epilogue_ref(M, N, C[np.ix_(rows, cols)], 2.0, 0.25, C_in=row_major.ravel(),
+    Db = epi(M, N, C[np.ix_(rows, cols)], 2.0, 0.25, C_in=row_major.ravel(),
                              ldc=N + 2, c_major=1, bias=bias, act="relu", rows=rows, cols=cols)
-    Df = oracle.epilogue_ref(M, N, C, 2.0, 0.25, C_in=row_major.ravel(), ldc=N + 2,
+    Df = epi(M, N, C, 2.0, 0.25, C_in=row_major.ravel(), ldc=N + 2,
                              c_major=1, bias=bias, act="relu")
     assert np.array_equal(Db, Df[np.ix_(rows, cols)])
+
+
+def test_epilogue_pins():
+    epilogue_pins(oracle.epilogue_ref)
 
 
 def test_epilogue_rejects_bad_arguments():
@@ -380,11 +386,13 @@ def test_epilogue_rejects_bad_arguments():
 # ------------------------------------------------------------ row softmax --
 # The Gluon Multi-CTA tutorial's multi-CTA softmax: y = exp(x - max) / sum.
 
-def test_softmax_pins():
+def softmax_pins(smx):
+    """Every softmax pin, against the callable `smx` (the oracle's
+    signature); raises AssertionError on the first that fails."""
     import math
     # hand-worked: x = [0, ln 2, ln 5] -> [1, 2, 5] / 8
     x = np.array([0.0, math.log(2.0), math.log(5.0)], np.float32)
-    y = oracle.softmax_ref(1, 3, x, 3)[0]
+    y = smx(1, 3, x, 3)[0]
     xd = x.astype(np.float64)
     want = np.exp(xd - xd.max()) / np.exp(xd - xd.max()).sum()
     assert np.allclose(y, want, rtol=1e-15, atol=0)
@@ -395,13 +403,13 @@ def test_softmax_pins():
     xs = np.full(M * ld, np.nan, np.float32)
     body = (rng.integers(-64, 64, (M, N)) / 8.0).astype(np.float32)  # exact under +16
     xs.reshape(M, ld)[:, :N] = body
-    y = oracle.softmax_ref(M, N, xs, ld)
+    y = smx(M, N, xs, ld)
     assert np.allclose(y.sum(axis=1), 1.0, rtol=0, atol=1e-14)
     shifted = xs.copy()
     shifted.reshape(M, ld)[:, :N] += 16.0
     assert np.array_equal(shifted.reshape(M, ld)[:, :N] - 16.0, body)
-    assert np.allclose(oracle.softmax_ref(M, N, shifted, ld), y, rtol=1e-13, atol=0)
-    assert np.allclose(oracle.softmax_ref(2, 9, np.full(18, 1.5, np.float32), 9), 1 / 9,
+    assert np.allclose(smx(M, N, shifted, ld), y, rtol=1e-13, atol=0)
+    assert np.allclose(smx(2, 9, np.full(18, 1.5, np.float32), 9), 1 / 9,
                        rtol=1e-15, atol=0)
     # monotone in x, and the largest input gets the largest output
     assert all(np.argmax(y[i]) == np.argmax(body[i]) for i in range(M))
@@ -410,5 +418,86 @@ def test_softmax_pins():
     # a dominant entry takes (almost) all the mass
     xd = np.zeros(50, np.float32)
     xd[7] = 60.0
-    yd = oracle.softmax_ref(1, 50, xd, 50)[0]
+    yd = smx(1, 50, xd, 50)[0]
     assert abs(yd[7] - 1.0) < 1e-24 and yd[0] == np.exp(-60.0) * yd[7]
+    # a large-magnitude row: without the max shift exp() overflows even in fp64
+    big = np.array([-5.0, 800.0, 3.0, 800.0], np.float32)
+    yb = smx(1, 4, big, 4)[0]
+    assert np.all(np.isfinite(yb)) and yb[1] == 0.5 and yb[3] == 0.5 and yb[0] == 0.0
+
+
+def test_softmax_pins():
+    softmax_pins(oracle.softmax_ref)
+
+
+# ---------------------------- planted mistakes in the epilogue and softmax --
+
+def _epilogue_mutant(kind):
+    """A plausible epilogue mistake, planted in a wrapper around the oracle."""
+    import math
+
+    def g(M, N, C_ref, alpha, beta, C_in=None, ldc=0, c_major=1, c_dtype="f32", bias=None,
+          act="none", rows=None, cols=None):
+        kw = dict(C_in=C_in, ldc=ldc, c_major=c_major, c_dtype=c_dtype, rows=rows, cols=cols)
+        if kind == "alpha_ignored":
+            return oracle.epilogue_ref(M, N, C_ref, 1.0, beta, bias=bias, act=act, **kw)
+        if kind == "beta_ignored":
+            return oracle.epilogue_ref(M, N, C_ref, alpha, 0.0, bias=bias, act=act, **kw)
+        if kind == "c_in_layout_swapped" and C_in is not None:
+            kw["c_major"] = 1 - c_major
+            return oracle.epilogue_ref(M, N, C_ref, alpha, beta, bias=bias, act=act, **kw)
+        if kind == "bias_by_row" and bias is not None and act == "none":
+            D = oracle.epilogue_ref(M, N, C_ref, alpha, beta, act=act, **kw)
+            r = np.arange(M) if rows is None else np.asarray(rows)
+            return D + np.asarray(bias, np.float64)[r % len(bias)][:, None]
+        if kind == "gelu_without_half" and act == "gelu":
+            pre = oracle.epilogue_ref(M, N, C_ref, alpha, beta, bias=bias, act="none", **kw)
+            return pre * (1.0 + np.vectorize(math.erf)(pre / math.sqrt(2.0)))
+        if kind == "relu_as_abs" and act == "relu":
+            pre = oracle.epilogue_ref(M, N, C_ref, alpha, beta, bias=bias, act="none", **kw)
+            return np.abs(pre)
+        return oracle.epilogue_ref(M, N, C_ref, alpha, beta, bias=bias, act=act, **kw)
+    return g
+
+
+@pytest.mark.parametrize("kind", ["alpha_ignored", "beta_ignored", "c_in_layout_swapped",
+                                  "bias_by_row", "gelu_without_half", "relu_as_abs"])
+def test_epilogue_pins_catch_planted_mistakes(kind):
+    with np.errstate(all="ignore"), pytest.raises(AssertionError):
+        epilogue_pins(_epilogue_mutant(kind))
+
+
+def _softmax_mutant(kind):
+    """A plausible softmax mistake, planted in a wrapper around the oracle."""
+    def rows_of(M, N, x, ldx):
+        x = np.asarray(x, np.float32)
+        return np.stack([x[m * ldx:m * ldx + N].astype(np.float64) for m in range(M)])
+
+    def g(M, N, x, ldx):
+        if kind == "no_max_shift":
+            e = np.exp(rows_of(M, N, x, ldx))
+            return e / e.sum(axis=1, keepdims=True)
+        if kind == "shift_by_first_value":
+            r = rows_of(M, N, x, ldx)
+            e = np.exp(r - r[:, :1])
+            return e / e.sum(axis=1, keepdims=True)
+        if kind == "not_normalised":
+            r = rows_of(M, N, x, ldx)
+            return np.exp(r - r.max(axis=1, keepdims=True))
+        if kind == "ld_ignored" and ldx != N:
+            return oracle.softmax_ref(M, N, x, N)
+        if kind == "last_column_dropped" and N > 1:
+            y = np.zeros((M, N))
+            xs = np.asarray(x, np.float32)
+            packed = np.concatenate([xs[m * ldx:m * ldx + N - 1] for m in range(M)])
+            y[:, :N - 1] = oracle.softmax_ref(M, N - 1, packed, N - 1)
+            return y
+        return oracle.softmax_ref(M, N, x, ldx)
+    return g
+
+
+@pytest.mark.parametrize("kind", ["no_max_shift", "shift_by_first_value", "not_normalised",
+                                  "ld_ignored", "last_column_dropped"])
+def test_softmax_pins_catch_planted_mistakes(kind):
+    with np.errstate(all="ignore"), pytest.raises(AssertionError):
+        softmax_pins(_softmax_mutant(kind))
