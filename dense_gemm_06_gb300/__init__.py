@@ -29,7 +29,7 @@ GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA, GEMM_ERR_TIM
     0, -1, -2, -3, -4
 GEMM_OPT_WAIT_LIMIT_NS, GEMM_OPT_TC_CTA_GROUP, GEMM_OPT_TC_FAULT_INJECT = 1, 2, 3
 GEMM_OPT_SIMT_CONFIG, GEMM_OPT_SIMT_TRANSPOSE, GEMM_OPT_TC_STORE = 4, 5, 6
-GEMM_OPT_TC_MULTICAST, GEMM_OPT_SOFTMAX_FAULT_INJECT = 7, 8
+GEMM_OPT_TC_MULTICAST, GEMM_OPT_SOFTMAX_FAULT_INJECT, GEMM_OPT_SIMT_SPLIT_TAIL = 7, 8, 9
 GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_GELU = 0, 1, 2
 
 

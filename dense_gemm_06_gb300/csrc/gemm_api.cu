@@ -35,6 +35,7 @@ std::atomic<int> g_fault_inject{0};
 std::atomic<int> g_softmax_fault_inject{0};
 std::atomic<int> g_simt_config{0};
 std::atomic<int> g_simt_transpose{0};
+std::atomic<int> g_simt_split{0};
 std::atomic<int> g_tc_store{0};
 std::atomic<int> g_tc_multicast{0};
 
@@ -47,6 +48,7 @@ struct RunConfig {
     int cta_group;       // 1 or 2
     int multicast;       // 1 off, 2 on
     int tc_store;        // 0 TMA where possible, 1 st.global
+    int simt_split;      // 0 automatic K-split of the last wave, 1 never, 2 always
 };
 
 // Problems gemm_tune() has measured: shape, types, layouts and whether each
@@ -278,7 +280,9 @@ int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCon
         *lds[i] = ld2;
         *kmaj[i] = false;
     }
-    if (rc == kOk) rc = launch_sgemm_f32(p, dev, cfg.simt_config, s);
+    Scratch tail{pool, s};
+    if (rc == kOk) rc = launch_sgemm_f32(p, dev, cfg.simt_config, cfg.simt_split, &tail, s);
+    if (tail.ptr) cudaFreeAsync(tail.ptr, s);
     for (int i = 0; i < 2; ++i)
         if (scratch[i]) cudaFreeAsync(scratch[i], s);
     return rc;
@@ -338,7 +342,7 @@ TuneKey make_key(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, in
 
 RunConfig resolve(const TuneKey& key) {
     RunConfig c{g_simt_config.load(), g_simt_transpose.load(), g_cta_group.load(),
-                g_tc_multicast.load(), g_tc_store.load()};
+                g_tc_multicast.load(), g_tc_store.load(), g_simt_split.load()};
     gemm_tuning t{};
     bool tuned = false;
     {
@@ -732,6 +736,10 @@ int gemm_set_option(int option, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             g_softmax_fault_inject.store((int)value);
             return GEMM_OK;
+        case GEMM_OPT_SIMT_SPLIT_TAIL:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_simt_split.store((int)value);
+            return GEMM_OK;
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -746,6 +754,7 @@ int64_t gemm_get_option(int option) {
         case GEMM_OPT_TC_STORE: return g_tc_store.load();
         case GEMM_OPT_TC_MULTICAST: return g_tc_multicast.load();
         case GEMM_OPT_SOFTMAX_FAULT_INJECT: return g_softmax_fault_inject.load();
+        case GEMM_OPT_SIMT_SPLIT_TAIL: return g_simt_split.load();
         default: return -1;
     }
 }

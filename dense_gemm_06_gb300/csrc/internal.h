@@ -44,7 +44,24 @@ struct DeviceInfo {
 // report through note_launch().
 // config: 0 = default tile configuration, 1..4 = a fixed one (see
 // GEMM_OPT_SIMT_CONFIG in gemm.h).
-int launch_sgemm_f32(const Problem& p, const DeviceInfo& dev, int config, cudaStream_t stream);
+// Stream-ordered scratch for one launch sequence: get() allocates once from
+// the pool; the caller frees `ptr` on the stream after the launches.
+struct Scratch {
+    cudaMemPool_t pool;
+    cudaStream_t stream;
+    void* ptr = nullptr;
+    void* get(size_t bytes) {
+        if (!ptr && cudaMallocFromPoolAsync(&ptr, bytes, pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            ptr = nullptr;
+        }
+        return ptr;
+    }
+};
+// split_mode: 0 automatic (K-split the last wave's tiles when it is at most
+// half full), 1 never, 2 always split the last wave (tests).
+int launch_sgemm_f32(const Problem& p, const DeviceInfo& dev, int config, int split_mode,
+                     Scratch* scratch, cudaStream_t stream);
 // dst[c * ldd + r] = src[r * lds + c] (fp32), rows x cols.
 int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
                          int64_t cols, const DeviceInfo& dev, cudaStream_t stream);

@@ -18,7 +18,12 @@
 //     shapes need no separate residue pass (the CuTe example shifts the
 //     ragged k-tile to the front instead; predicating every copy costs a few
 //     integer compares per k-tile here and keeps one code path);
-//   * predicated epilogue with 128-bit stores when C allows them.
+//   * predicated epilogue with 128-bit stores when C allows them;
+//   * wave tail: when the last wave of CTAs would leave at least half of the
+//     CTA slots idle, the tiles of that wave are split along K into `splits`
+//     slices computed by separate CTAs, which store raw partial sums in pool
+//     scratch; a fixup kernel adds the slices in slice order and runs the
+//     normal epilogue, so the last wave takes 1/splits of the time.
 #include <atomic>
 #include <cstdint>
 
@@ -60,7 +65,72 @@ struct SgemmParams {
     int tiles_m, tiles_n;
     int c_vec;
     EpiParams epi;  // fused epilogue (inactive for a plain GEMM)
+    int dp_tiles;   // tiles 0 .. dp_tiles-1 (raster order) are computed whole
+    int splits;     // K-slices of each later tile (one CTA per slice)
+    int kt_slice;   // k-tiles per slice
+    float* ws;      // raw partial tiles of the slices: [unit][16][THREADS] float4
 };
+
+// Raster: bands of BAND tile-rows, walking down M inside a band first.
+__device__ __forceinline__ void tile_origin(const SgemmParams& p, int t, int& m0, int& n0) {
+    const int band_tiles = BAND * p.tiles_n;
+    const int band = t / band_tiles;
+    const int within = t - band * band_tiles;
+    const int m_lo = band * BAND;
+    const int rows_in_band = min(BAND, p.tiles_m - m_lo);
+    m0 = (m_lo + within % rows_in_band) * BM;
+    n0 = (within / rows_in_band) * BN;
+}
+
+// Thread -> C block: warp (wy, wx) = (w / 2, w % 2), lane (ly, lx) =
+// (l / 8, l % 8); ty in 0..15, tx in 0..15. The thread owns rows
+// ty*4 + (i & 3) + (i >> 2) * 64 and columns tx*4 + (c & 3) + (c >> 2) * 64.
+__device__ __forceinline__ void thread_block(int tid, int& ty, int& tx) {
+    const int w = tid >> 5, l = tid & 31;
+    ty = (w >> 1) * 4 + (l >> 3);
+    tx = (w & 1) * 8 + (l & 7);
+}
+
+// Stores the thread's 8 x 8 block of the tile at (m0, n0), applying the fused
+// epilogue when one is active; predicated on M and N.
+__device__ __forceinline__ void store_block(const SgemmParams& p, const float2 (&acc)[8][4],
+                                            int m0, int n0, int ty, int tx) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = m0 + ty * 4 + (i & 3) + (i >> 2) * 64;
+        if (row >= p.M) continue;
+        float* crow = p.C + (int64_t)row * p.ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = n0 + tx * 4 + h * 64;
+            float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                          acc[i][2 * h + 1].y};
+            if (p.epi.active) {  // D = act(alpha * acc + beta * C_old + bias)
+                float old[4] = {0.f, 0.f, 0.f, 0.f};
+                if (p.epi.beta != 0.f) {
+                    if (p.c_vec && col + 3 < p.N) {
+                        const float4 o = *reinterpret_cast<const float4*>(crow + col);
+                        old[0] = o.x; old[1] = o.y; old[2] = o.z; old[3] = o.w;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (col + j < p.N) old[j] = crow[col + j];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < p.N) v[j] = epilogue_value<float>(p.epi, v[j], old[j], row, col + j);
+            }
+            if (p.c_vec && col + 3 < p.N) {
+                *reinterpret_cast<float4*>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < p.N) crow[col + j] = v[j];
+            }
+        }
+    }
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -99,32 +169,33 @@ struct TileLoader {
                          // the vector; MN 4B: 1 if the row is valid
     uint32_t s_off;      // byte offset of its first element inside a stage
 
+    // k0: first k of the first tile this CTA loads (a multiple of BK).
     __device__ __forceinline__ void init(const float* X, int64_t ld_, int R, int K, int r0,
-                                         int tid) {
+                                         int k0, int tid) {
         ld = ld_;
         rows_ok = 0;
         if constexpr (KMAJOR) {
             // element e = tid + 256 i: k-group h = e >> 10, row = (e & 1023) >> 3,
             // k = 8 h + (e & 7); a thread's rows are (tid >> 3) + 32 q.
             const int rr = tid >> 3, kk = tid & 7;
-            ptr = X + (int64_t)(r0 + rr) * ld + kk;
-            k_left = K - kk;
+            ptr = X + (int64_t)(r0 + rr) * ld + k0 + kk;
+            k_left = K - k0 - kk;
             s_off = (uint32_t)(kk * LDS + rr) * 4u;
 #pragma unroll
             for (int q = 0; q < 4; ++q) rows_ok |= (r0 + rr + 32 * q < R) << q;
         } else if constexpr (VEC == 4) {
             // float4 idx = tid + 256 i: k = (tid >> 5) + 8 i, rows 4 (tid & 31) ..
             const int rr = (tid & 31) << 2, kk = tid >> 5;
-            ptr = X + (int64_t)kk * ld + r0 + rr;
-            k_left = K - kk;
+            ptr = X + (int64_t)(k0 + kk) * ld + r0 + rr;
+            k_left = K - k0 - kk;
             s_off = (uint32_t)(kk * LDS + rr) * 4u;
             const int v = R - (r0 + rr);
             rows_ok = v >= 4 ? 4 : (v > 0 ? v : 0);
         } else {
             // element e = tid + 256 i: k = (tid >> 7) + 2 i, row = tid & 127
             const int rr = tid & 127, kk = tid >> 7;
-            ptr = X + (int64_t)kk * ld + r0 + rr;
-            k_left = K - kk;
+            ptr = X + (int64_t)(k0 + kk) * ld + r0 + rr;
+            k_left = K - k0 - kk;
             s_off = (uint32_t)(kk * LDS + rr) * 4u;
             rows_ok = (r0 + rr < R) ? 1 : 0;
         }
@@ -172,30 +243,25 @@ __global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const Sg
     extern __shared__ __align__(16) float smem[];
     const int tid = threadIdx.x;
 
-    // Raster: bands of BAND tile-rows, walking down M inside a band first.
-    const int t = blockIdx.x;
-    const int band_tiles = BAND * p.tiles_n;
-    const int band = t / band_tiles;
-    const int within = t - band * band_tiles;
-    const int m_lo = band * BAND;
-    const int rows_in_band = min(BAND, p.tiles_m - m_lo);
-    const int tm = m_lo + within % rows_in_band;
-    const int tn = within / rows_in_band;
-    const int m0 = tm * BM, n0 = tn * BN;
-
-    // Thread -> C block: warp (wy, wx) = (w / 2, w % 2), lane (ly, lx) =
-    // (l / 8, l % 8); ty in 0..15, tx in 0..15.
-    const int w = tid >> 5, l = tid & 31;
-    const int ty = (w >> 1) * 4 + (l >> 3);
-    const int tx = (w & 1) * 8 + (l & 7);
+    // CTA -> tile (and K-slice for the split tail).
+    int t = blockIdx.x, kt0 = 0;
+    int nkt = (p.K + BK - 1) / BK;
+    if (t >= p.dp_tiles) {
+        const int unit = t - p.dp_tiles;
+        t = p.dp_tiles + unit / p.splits;
+        kt0 = (unit % p.splits) * p.kt_slice;
+        nkt = max(0, min(nkt, kt0 + p.kt_slice) - kt0);
+    }
+    int m0, n0, ty, tx;
+    tile_origin(p, t, m0, n0);
+    thread_block(tid, ty, tx);
 
     const uint32_t s0 = smem_addr(smem);
-    const int nkt = (p.K + BK - 1) / BK;
 
     TileLoader<BK, A_K, A_VEC> la;
     TileLoader<BK, B_K, B_VEC> lb;
-    la.init(p.A, p.lda, p.M, p.K, m0, tid);
-    lb.init(p.B, p.ldb, p.N, p.K, n0, tid);
+    la.init(p.A, p.lda, p.M, p.K, m0, kt0 * BK, tid);
+    lb.init(p.B, p.ldb, p.N, p.K, n0, kt0 * BK, tid);
     // Tiles are issued strictly in order kt = 0, 1, 2, ...
     auto load_stage = [&](int stage) {
         const uint32_t sa = s0 + (uint32_t)(stage * Cfg::STAGE_FLOATS) * 4u;
@@ -257,42 +323,52 @@ __global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const Sg
     }
     cp_async_wait<0>();
 
-    // Epilogue: rows ty*4 + (i & 3) + (i >> 2) * 64, cols tx*4 + (j & 3) + (j >> 2) * 64.
+    if ((int)blockIdx.x >= p.dp_tiles) {  // a K-slice of a tail tile: raw partial sums
+        const int unit = (int)blockIdx.x - p.dp_tiles;
+        float4* wsp = reinterpret_cast<float4*>(p.ws) + (size_t)unit * (16 * THREADS) + tid;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = m0 + ty * 4 + (i & 3) + (i >> 2) * 64;
-        if (row >= p.M) continue;
-        float* crow = p.C + (int64_t)row * p.ldc;
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                wsp[(2 * i + h) * THREADS] = make_float4(acc[i][2 * h].x, acc[i][2 * h].y,
+                                                         acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+        return;
+    }
+    store_block(p, acc, m0, n0, ty, tx);
+}
+
+// Tail fixup: tile dp_tiles + blockIdx.x = the sum of its K-slices' partial
+// tiles, added in slice order, then the normal epilogue.
+__global__ void __launch_bounds__(THREADS) sgemm_split_fixup_kernel(const SgemmParams p) {
+    const int tid = threadIdx.x;
+    int m0, n0, ty, tx;
+    tile_origin(p, p.dp_tiles + blockIdx.x, m0, n0);
+    thread_block(tid, ty, tx);
+    const float4* wsp = reinterpret_cast<const float4*>(p.ws) +
+                        (size_t)blockIdx.x * p.splits * (16 * THREADS) + tid;
+    float2 acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int col = n0 + tx * 4 + h * 64;
-            float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
-                          acc[i][2 * h + 1].y};
-            if (p.epi.active) {  // D = act(alpha * acc + beta * C_old + bias)
-                float old[4] = {0.f, 0.f, 0.f, 0.f};
-                if (p.epi.beta != 0.f) {
-                    if (p.c_vec && col + 3 < p.N) {
-                        const float4 o = *reinterpret_cast<const float4*>(crow + col);
-                        old[0] = o.x; old[1] = o.y; old[2] = o.z; old[3] = o.w;
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (col + j < p.N) old[j] = crow[col + j];
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (col + j < p.N) v[j] = epilogue_value<float>(p.epi, v[j], old[j], row, col + j);
-            }
-            if (p.c_vec && col + 3 < p.N) {
-                *reinterpret_cast<float4*>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (col + j < p.N) crow[col + j] = v[j];
-            }
+            const float4 q = wsp[(2 * i + h) * THREADS];
+            acc[i][2 * h] = make_float2(q.x, q.y);
+            acc[i][2 * h + 1] = make_float2(q.z, q.w);
         }
+    for (int sl = 1; sl < p.splits; ++sl) {
+        const float4* w = wsp + (size_t)sl * (16 * THREADS);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 q = w[(2 * i + h) * THREADS];
+                acc[i][2 * h].x += q.x;
+                acc[i][2 * h].y += q.y;
+                acc[i][2 * h + 1].x += q.z;
+                acc[i][2 * h + 1].y += q.w;
+            }
     }
+    store_block(p, acc, m0, n0, ty, tx);
 }
 
 // Sets the dynamic shared-memory limit of `kern` once per device; `done` is
@@ -308,22 +384,83 @@ bool configure_once(Kern kern, std::atomic<uint64_t>& done, int device, int smem
     return true;
 }
 
+// Chooses the split of the last wave: with S resident CTAs and T tiles, a
+// last wave of r = T mod S tiles (T >= S) that fills at most half of the
+// slots is cut into s = min(4, S / r) K-slices per tile (each slice at least
+// 4 k-tiles); split_mode 2 always cuts the last wave (all tiles if T < S)
+// into at least 2 slices.
+void plan_split(SgemmParams& sp, int slots, int nkt, int split_mode) {
+    const int64_t T = (int64_t)sp.tiles_m * sp.tiles_n;
+    sp.dp_tiles = (int)T;
+    sp.splits = 1;
+    sp.kt_slice = nkt;
+    if (split_mode == 1 || slots <= 0 || T <= 0) return;
+    int64_t r = T % slots;
+    if (split_mode == 2) {
+        if (r == 0) r = T < slots ? T : slots;
+        int s = (int)(slots / r);
+        s = s < 2 ? 2 : (s > 4 ? 4 : s);
+        sp.dp_tiles = (int)(T - r);
+        sp.splits = s;
+        sp.kt_slice = (nkt + s - 1) / s;
+        return;
+    }
+    if (T < slots || r == 0 || 2 * r > slots) return;
+    int s = (int)(slots / r);
+    if (s > 4) s = 4;
+    while (s > 1 && nkt < 4 * s) --s;
+    if (s < 2) return;
+    sp.dp_tiles = (int)(T - r);
+    sp.splits = s;
+    sp.kt_slice = (nkt + s - 1) / s;
+}
+
 template <class Cfg, bool A_K, int A_VEC, bool B_K, int B_VEC>
-int launch_variant(const SgemmParams& sp, int device, cudaStream_t stream) {
+int launch_variant(SgemmParams sp, int device, int sm_count, int split_mode, Scratch* scratch,
+                   cudaStream_t stream) {
     auto kern = sgemm_ffma_kernel<Cfg, A_K, A_VEC, B_K, B_VEC>;
     static std::atomic<uint64_t> configured{0};  // per kernel variant
+    static std::atomic<int> per_sm[64];           // resident CTAs per SM, per device
     if (!configure_once(kern, configured, device, Cfg::SMEM_BYTES)) return kCuda;
-    const int64_t tiles = (int64_t)sp.tiles_m * sp.tiles_n;
-    kern<<<dim3((unsigned)tiles), dim3(THREADS), Cfg::SMEM_BYTES, stream>>>(sp);
+    int occ = per_sm[device & 63].load();
+    if (occ == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS,
+                                                          Cfg::SMEM_BYTES) != cudaSuccess) {
+            cudaGetLastError();
+            occ = -1;
+        }
+        per_sm[device & 63].store(occ);
+    }
+    plan_split(sp, occ > 0 ? occ * sm_count : 0, (sp.K + Cfg::BK - 1) / Cfg::BK, split_mode);
+    const int64_t tail = (int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles;
+    if (tail > 0) {
+        const size_t bytes = (size_t)tail * sp.splits * BM * BN * sizeof(float);
+        sp.ws = scratch ? static_cast<float*>(scratch->get(bytes)) : nullptr;
+        if (!sp.ws) {  // no scratch: compute every tile whole
+            sp.dp_tiles = sp.tiles_m * sp.tiles_n;
+            sp.splits = 1;
+        }
+    }
+    const int64_t units = sp.dp_tiles + ((int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles) * sp.splits;
+    kern<<<dim3((unsigned)units), dim3(THREADS), Cfg::SMEM_BYTES, stream>>>(sp);
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     note_launch();
+    const int64_t fix = (int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles;
+    if (fix > 0) {
+        sgemm_split_fixup_kernel<<<dim3((unsigned)fix), dim3(THREADS), 0, stream>>>(sp);
+        if (cudaGetLastError() != cudaSuccess) return kCuda;
+        note_launch();
+    }
     return kOk;
 }
 
 template <class Cfg>
-int launch_layout(const SgemmParams& sp, int av, int bv, int device, cudaStream_t s) {
-#define SG_CASE(AV, BV, AK, AVEC, BK_, BVEC) \
-    if (av == AV && bv == BV) return launch_variant<Cfg, AK, AVEC, BK_, BVEC>(sp, device, s);
+int launch_layout(const SgemmParams& sp, int av, int bv, int device, int sm_count, int split_mode,
+                  Scratch* scratch, cudaStream_t s) {
+#define SG_CASE(AV, BV, AK, AVEC, BK_, BVEC)                                                   \
+    if (av == AV && bv == BV)                                                                  \
+        return launch_variant<Cfg, AK, AVEC, BK_, BVEC>(sp, device, sm_count, split_mode,      \
+                                                        scratch, s);
     SG_CASE(0, 0, true, 1, true, 1)
     SG_CASE(0, 4, true, 1, false, 4)
     SG_CASE(0, 1, true, 1, false, 1)
@@ -383,7 +520,8 @@ int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd,
     return kOk;
 }
 
-int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, cudaStream_t stream) {
+int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, int split_mode,
+                     Scratch* scratch, cudaStream_t stream) {
     SgemmParams sp;
     sp.A = static_cast<const float*>(pr.A);
     sp.B = static_cast<const float*>(pr.B);
@@ -398,18 +536,23 @@ int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, cudaS
     sp.tiles_n = (int)((pr.N + BN - 1) / BN);
     sp.c_vec = aligned16(pr.C, pr.ldc) ? 1 : 0;
     sp.epi = pr.epi;
-    if ((int64_t)sp.tiles_m * sp.tiles_n > 0x7fffffffLL) return kUnsupported;
+    sp.dp_tiles = 0;
+    sp.splits = 1;
+    sp.kt_slice = 0;
+    sp.ws = nullptr;
+    if ((int64_t)sp.tiles_m * sp.tiles_n > 0x3fffffffLL) return kUnsupported;
 
     // A/B variant: K-major (4-byte transposing copies), MN-major 16-byte or 4-byte.
     const int av = pr.a_kmajor ? 0 : (aligned16(pr.A, pr.lda) ? 4 : 1);
     const int bv = pr.b_kmajor ? 0 : (aligned16(pr.B, pr.ldb) ? 4 : 1);
+    const int d = dev.device, n = dev.sm_count;
     switch (config) {
-        case 2: return launch_layout<SgCfg<16, 4, false, 2>>(sp, av, bv, dev.device, stream);
-        case 3: return launch_layout<SgCfg<32, 3, true, 2>>(sp, av, bv, dev.device, stream);
-        case 4: return launch_layout<SgCfg<8, 3, true, 2>>(sp, av, bv, dev.device, stream);
-        case 5: return launch_layout<SgCfg<16, 4, true, 1>>(sp, av, bv, dev.device, stream);
-        case 6: return launch_layout<SgCfg<32, 4, true, 1>>(sp, av, bv, dev.device, stream);
-        default: return launch_layout<SgCfg<16, 4, true, 2>>(sp, av, bv, dev.device, stream);
+        case 2: return launch_layout<SgCfg<16, 4, false, 2>>(sp, av, bv, d, n, split_mode, scratch, stream);
+        case 3: return launch_layout<SgCfg<32, 3, true, 2>>(sp, av, bv, d, n, split_mode, scratch, stream);
+        case 4: return launch_layout<SgCfg<8, 3, true, 2>>(sp, av, bv, d, n, split_mode, scratch, stream);
+        case 5: return launch_layout<SgCfg<16, 4, true, 1>>(sp, av, bv, d, n, split_mode, scratch, stream);
+        case 6: return launch_layout<SgCfg<32, 4, true, 1>>(sp, av, bv, d, n, split_mode, scratch, stream);
+        default: return launch_layout<SgCfg<16, 4, true, 2>>(sp, av, bv, d, n, split_mode, scratch, stream);
     }
 }
 

@@ -318,7 +318,15 @@ enum gemm_option {
        its partial, so that row's CTAs wait out GEMM_OPT_WAIT_LIMIT_NS and
        report GEMM_ERR_TIMEOUT through gemm_check_device_error; the row's y
        is then undefined. 0 (default) = off. */
-    GEMM_OPT_SOFTMAX_FAULT_INJECT = 8
+    GEMM_OPT_SOFTMAX_FAULT_INJECT = 8,
+    /* Wave tail of the fp32 FFMA kernel: 0 = automatic (when the last wave of
+       128 x 128 tiles would fill at most half of the resident CTA slots, its
+       tiles are split along K into 2-4 slices computed by separate CTAs into
+       pool scratch and summed in slice order by a fixup kernel before the
+       epilogue), 1 = never split, 2 = always split the last wave (every tile
+       when there is less than one wave). A split changes the order of the
+       k-sum, never the per-product rounding. */
+    GEMM_OPT_SIMT_SPLIT_TAIL = 9
 };
 
 /* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */

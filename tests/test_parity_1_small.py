@@ -182,3 +182,30 @@ def test_sgemm_with_and_without_operand_transpose(transpose, am, bm, cm):
         run_and_check(64, 96, 33, lg.GEMM_F32, am, bm, cm, dist="int", seed=12)
     finally:
         lg.gemm_set_option(lg.GEMM_OPT_SIMT_TRANSPOSE, old)
+
+
+# K-split of the FFMA kernel's last wave (GEMM_OPT_SIMT_SPLIT_TAIL): forced on
+# small and ragged shapes (every tile split, slices of one k-tile or empty),
+# and the automatic rule on a shape whose last wave is nearly empty.
+@pytest.mark.parametrize("config", [1, 5])
+@pytest.mark.parametrize("am,bm,cm", list(itertools.product((0, 1), (0, 1), (0, 1))))
+def test_sgemm_split_tail_forced(config, am, bm, cm):
+    old = {o: lg.gemm_get_option(o) for o in (lg.GEMM_OPT_SIMT_SPLIT_TAIL,
+                                              lg.GEMM_OPT_SIMT_CONFIG)}
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 2))
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, config))
+    try:
+        for i, (M, N, K) in enumerate([(1, 1, 1), (15, 17, 7), (130, 260, 300), (257, 131, 33)]):
+            run_and_check(M, N, K, lg.GEMM_F32, am, bm, cm, dist="int", seed=40 + i,
+                          lda_pad=i % 2, ldc_pad=i % 3)
+        run_and_check(300, 520, 200, lg.GEMM_F32, am, bm, cm, dist="pm1", seed=45)
+    finally:
+        for o, v in old.items():
+            lg.gemm_set_option(o, v)
+
+
+@pytest.mark.parametrize("am,bm", [(0, 0), (1, 1)])
+def test_sgemm_split_tail_automatic(am, bm):
+    # 20 x 16 = 320 tiles on 2 x 152 CTA slots: a 16-tile last wave, split 4 ways
+    assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL) == 0
+    run_and_check(2557, 2043, 300, lg.GEMM_F32, am, bm, 1, dist="int", seed=46)

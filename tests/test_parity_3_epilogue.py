@@ -109,3 +109,15 @@ def test_gemm_ex_k_zero(dtype):
 def test_gemm_ex_plain_is_gemm():
     # alpha 1, beta 0, no bias, no activation: the plain gemm() path
     run_ex(300, 520, 200, lg.GEMM_BF16_F32, 0, 0, 1, "none", 1.0, 0.0, False, seed=26)
+
+
+@pytest.mark.parametrize("act", sorted(ACTS))
+def test_gemm_ex_with_split_tail(act):
+    # the fixup kernel of the FFMA kernel's K-split applies the epilogue
+    old = lg.gemm_get_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL)
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 2))
+    try:
+        run_ex(300, 261, 70, lg.GEMM_F32, 0, 1, 1, act, 0.5, 0.25, True, seed=31, ldc_pad=3)
+        run_ex(130, 77, 40, lg.GEMM_F32, 1, 0, 0, act, -1.0, 0.0, False, seed=32)
+    finally:
+        lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, old)
