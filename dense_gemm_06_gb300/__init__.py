@@ -30,6 +30,7 @@ GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA, GEMM_ERR_TIM
 GEMM_OPT_WAIT_LIMIT_NS, GEMM_OPT_TC_CTA_GROUP, GEMM_OPT_TC_FAULT_INJECT = 1, 2, 3
 GEMM_OPT_SIMT_CONFIG, GEMM_OPT_SIMT_TRANSPOSE, GEMM_OPT_TC_STORE = 4, 5, 6
 GEMM_OPT_TC_MULTICAST, GEMM_OPT_SOFTMAX_FAULT_INJECT, GEMM_OPT_SIMT_SPLIT_TAIL = 7, 8, 9
+GEMM_OPT_TC_SCHEDULER = 10
 GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_GELU = 0, 1, 2
 
 
@@ -37,7 +38,8 @@ class GemmTuning(ctypes.Structure):
     """struct gemm_tuning: the configuration gemm_tune chose."""
     _fields_ = [("simt_config", ctypes.c_int), ("simt_transpose", ctypes.c_int),
                 ("tc_cta_group", ctypes.c_int), ("tc_multicast", ctypes.c_int),
-                ("tc_store", ctypes.c_int), ("ms", ctypes.c_float), ("candidates", ctypes.c_int)]
+                ("tc_store", ctypes.c_int), ("ms", ctypes.c_float), ("candidates", ctypes.c_int),
+                ("tc_scheduler", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -36,6 +36,7 @@ std::atomic<int> g_softmax_fault_inject{0};
 std::atomic<int> g_simt_config{0};
 std::atomic<int> g_simt_transpose{0};
 std::atomic<int> g_simt_split{0};
+std::atomic<int> g_tc_scheduler{0};
 std::atomic<int> g_tc_store{0};
 std::atomic<int> g_tc_multicast{0};
 
@@ -49,6 +50,7 @@ struct RunConfig {
     int multicast;       // 1 off, 2 on
     int tc_store;        // 0 TMA where possible, 1 st.global
     int simt_split;      // 0 automatic K-split of the last wave, 1 never, 2 always
+    int tc_scheduler;    // 1 static persistent, 2 cluster launch control
 };
 
 // Problems gemm_tune() has measured: shape, types, layouts and whether each
@@ -321,7 +323,8 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCo
     }
     if (rc == kOk)
         rc = launch_gemm_tc(p, dev, cfg.cta_group, g_wait_limit_ns.load(),
-                            g_fault_inject.load(), cfg.tc_store != 1, cfg.multicast == 2, s);
+                            g_fault_inject.load(), cfg.tc_store != 1, cfg.multicast == 2,
+                            cfg.tc_scheduler == 2, s);
     for (int i = 0; i < 2; ++i)
         if (scratch[i]) cudaFreeAsync(scratch[i], s);
     return rc;
@@ -342,7 +345,8 @@ TuneKey make_key(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, in
 
 RunConfig resolve(const TuneKey& key) {
     RunConfig c{g_simt_config.load(), g_simt_transpose.load(), g_cta_group.load(),
-                g_tc_multicast.load(), g_tc_store.load(), g_simt_split.load()};
+                g_tc_multicast.load(), g_tc_store.load(), g_simt_split.load(),
+                g_tc_scheduler.load()};
     gemm_tuning t{};
     bool tuned = false;
     {
@@ -358,6 +362,7 @@ RunConfig resolve(const TuneKey& key) {
     if (c.cta_group == 0) c.cta_group = tuned && t.tc_cta_group ? t.tc_cta_group : 2;
     if (c.multicast == 0) c.multicast = tuned && t.tc_multicast ? t.tc_multicast : 1;
     if (c.tc_store == 0 && tuned) c.tc_store = t.tc_store;
+    if (c.tc_scheduler == 0) c.tc_scheduler = tuned && t.tc_scheduler ? t.tc_scheduler : 1;
     return c;
 }
 
@@ -572,10 +577,11 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
                 for (int t = 1; t <= (any_kmajor ? 2 : 1); ++t) cands[n++] = {c, t, 2, 1, 0};
         } else {
             const bool c_aligned = aligned16_ld(C, ldc, out_bytes(dtype));
-            const int modes[3][2] = {{1, 1}, {2, 1}, {2, 2}};
+            // (CTA group, multicast, scheduler); multicast runs the static one
+            const int modes[5][3] = {{1, 1, 1}, {1, 1, 2}, {2, 1, 1}, {2, 1, 2}, {2, 2, 1}};
             for (const auto& m : modes)
                 for (int st = c_aligned ? 0 : 1; st <= 1; ++st)
-                    cands[n++] = {1, 0, m[0], m[1], st};
+                    cands[n++] = {1, 0, m[0], m[1], st, 0, m[2]};
         }
 
         cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -610,7 +616,8 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
             return rc;
         }
         best = gemm_tuning{best_cfg.simt_config, best_cfg.simt_transpose, best_cfg.cta_group,
-                           best_cfg.multicast, best_cfg.tc_store, best_ms, n};
+                           best_cfg.multicast, best_cfg.tc_store, best_ms, n,
+                           best_cfg.tc_scheduler};
         {
             std::lock_guard<std::mutex> lock(g_tune_mu);
             g_tune_table[make_key(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major,
@@ -740,6 +747,10 @@ int gemm_set_option(int option, int64_t value) {
             if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             g_simt_split.store((int)value);
             return GEMM_OK;
+        case GEMM_OPT_TC_SCHEDULER:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_tc_scheduler.store((int)value);
+            return GEMM_OK;
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -755,6 +766,7 @@ int64_t gemm_get_option(int option) {
         case GEMM_OPT_TC_MULTICAST: return g_tc_multicast.load();
         case GEMM_OPT_SOFTMAX_FAULT_INJECT: return g_softmax_fault_inject.load();
         case GEMM_OPT_SIMT_SPLIT_TAIL: return g_simt_split.load();
+        case GEMM_OPT_TC_SCHEDULER: return g_tc_scheduler.load();
         default: return -1;
     }
 }

@@ -185,7 +185,8 @@ extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int6
                               (uint64_t)(wait > 0 ? wait : 1000000000ll),
                               (int)gemm_get_option(GEMM_OPT_TC_FAULT_INJECT),
                               gemm_get_option(GEMM_OPT_TC_STORE) != 1,
-                              gemm_get_option(GEMM_OPT_TC_MULTICAST) == 2, s);
+                              gemm_get_option(GEMM_OPT_TC_MULTICAST) == 2,
+                              gemm_get_option(GEMM_OPT_TC_SCHEDULER) == 2, s);
     } catch (...) {
         return kCuda;
     }

@@ -62,6 +62,7 @@ constexpr int TMEM_COLS = 512;   // two accumulators
 constexpr int THREADS = 256;
 constexpr int EPI_WARP0 = 4;     // epilogue warps 4..7 (warp % 4 == TMEM lane quarter)
 constexpr int BAND = 8;          // tile rows per raster band
+constexpr int CLC_SLOTS = 3;     // cluster-launch-control responses in flight
 
 template <int CG> struct Cfg {
     static constexpr int B_ROWS = TILE_N / CG;            // B rows (N) held per CTA
@@ -72,9 +73,11 @@ template <int CG> struct Cfg {
     static constexpr int TILE_M = ROWS_A * CG;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     // barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain, never,
-    // then the TMEM address slot
-    static constexpr int NUM_BARS = 2 * STAGES + 6;
-    static constexpr int BAR_BYTES = NUM_BARS * 8 + 8;
+    // clc_ready[CLC_SLOTS], clc_consumed[CLC_SLOTS], then the TMEM address
+    // slot, padding, and the 16-byte CLC responses
+    static constexpr int NUM_BARS = 2 * STAGES + 6 + 2 * CLC_SLOTS;
+    static constexpr int RESP_OFFSET = (NUM_BARS * 8 + 8 + 15) / 16 * 16;
+    static constexpr int BAR_BYTES = RESP_OFFSET + 16 * CLC_SLOTS;
     // epilogue staging: one 32 x 128-byte tile per epilogue warp
     static constexpr int EPI_BYTES = 4 * 32 * 128;
     static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + align slack
@@ -93,6 +96,7 @@ struct TcParams {
     unsigned int* err;         // device error word
     unsigned long long wait_limit_ns;
     int fault_inject;          // test hook: 1 = epilogue waits on a barrier nobody arrives at
+    int clc;                   // 1: one cluster per tile, later tiles taken by try_cancel
     EpiParams epi;             // fused epilogue (inactive for a plain GEMM)
 };
 
@@ -352,6 +356,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     auto acce_bar = [&](int a) { return bar0 + 8u * (2 * C_::STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * C_::STAGES + 4);
     const uint32_t never_bar = bar0 + 8u * (2 * C_::STAGES + 5);  // nothing ever arrives
+    auto ready_bar = [&](int s) { return bar0 + 8u * (2 * C_::STAGES + 6 + s); };
+    auto cons_bar = [&](int s) { return bar0 + 8u * (2 * C_::STAGES + 6 + CLC_SLOTS + s); };
+    auto resp_addr = [&](int s) { return bar0 + (uint32_t)(C_::RESP_OFFSET + 16 * s); };
     uint32_t* tmem_slot =
         reinterpret_cast<uint32_t*>(smem + C_::RING_BYTES + C_::EPI_BYTES + 8 * C_::NUM_BARS);
 
@@ -372,6 +379,31 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         if (MC) tc.tm = tc.tm * 2 + pair;  // may be past the last tile row: all rows OOB
         return tc;
     };
+    // Next tile of a role (t = total_tiles: no more work). Static schedule:
+    // every nclusters-th tile. CLC: the j-th response of the scheduler ring
+    // (the tile of a cluster it cancelled), which the role then releases to
+    // the pair leader's consumed barrier. warp_wide: all lanes of the warp
+    // call it and one arrives. False when a wait ran out.
+    auto advance = [&](int& t, int& j, bool warp_wide) -> bool {
+        if (!p.clc) {
+            t += nclusters;
+            return true;
+        }
+        const int s = j % CLC_SLOTS;
+        bool ok = wait_bar(ready_bar(s), (uint32_t)((j / CLC_SLOTS) & 1), p);
+        if (warp_wide) ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        int x = 0;
+        const bool more = clc_query(resp_addr(s), &x);
+        if (warp_wide) __syncwarp();
+        if (!warp_wide || (threadIdx.x & 31) == 0) {
+            if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(cons_bar(s), lead));
+            else mbar_arrive_local(cons_bar(s));
+        }
+        ++j;
+        t = more ? x / CG : total_tiles;
+        return true;
+    };
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&p.tmap_a);
@@ -386,6 +418,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         }
         mbar_init(drain_bar, 1);
         mbar_init(never_bar, 1);
+        for (int s = 0; s < CLC_SLOTS; ++s) {
+            mbar_init(ready_bar(s), 1);  // this CTA's scheduler thread arms it
+            // consumers of the pair: producers, the MMA thread, epilogue warps
+            mbar_init(cons_bar(s), CG == 2 ? 11 : 6);
+        }
         fence_mbarrier_init_cluster();
     }
     if (warp == 1) {
@@ -404,7 +441,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
+            int j = 0;
+            for (int t = cluster; t < total_tiles && !aborted;) {
                 const TileCoord tc = tile_of(t);
                 const int a_row = tc.tm * C_::TILE_M + (int)rank * ROWS_A;
                 const int b_row = tc.tn * TILE_N + (int)rank * C_::B_ROWS;
@@ -440,6 +478,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                     }
                     if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
                 }
+                if (aborted || !advance(t, j, false)) { aborted = true; break; }
             }
             if (aborted) grace_period_ns(200000);  // let issued copies land
         }
@@ -453,7 +492,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
+            int j = 0;
+            for (int t = cluster; t < total_tiles && !aborted;) {
                 if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, p)) { aborted = true; break; }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
@@ -482,6 +522,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 if constexpr (MC) mma_commit_pair(accf_bar(acc), (uint16_t)(0x3u << (2 * pair)));
                 else mma_commit<CG>(accf_bar(acc));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                if (!advance(t, j, false)) { aborted = true; break; }
             }
             // Drain: wait (bounded) until every MMA issued above has completed.
             if constexpr (CG == 2) mma_commit_pair(drain_bar, (uint16_t)(1u << crank));
@@ -502,7 +543,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             // Test hook: a wait that nothing completes must time out cleanly.
             if (!__all_sync(0xffffffffu, wait_bar(never_bar, 0u, p))) aborted = true;
         }
-        for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
+        int j = 0;
+        for (int t = cluster; t < total_tiles && !aborted;) {
             const TileCoord tc = tile_of(t);
             if (!__all_sync(0xffffffffu, wait_bar(accf_bar(acc), acc_phase, p))) {
                 aborted = true;
@@ -526,8 +568,36 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 else mbar_arrive_local(acce_bar(acc));
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (!advance(t, j, true)) { aborted = true; break; }
         }
         if (p.c_tma && lane == 0) bulk_wait_all();  // stores done before the CTA exits
+        __syncwarp();
+    } else if (warp == 2) {
+        // --------------------------------------- tile scheduler (CLC) --
+        // Each CTA arms its own ready barrier for every response; the pair
+        // leader issues the requests (multicast to both CTAs), each one into
+        // a slot that every consumer of the pair has released, and stops
+        // after the first response that cancelled nothing.
+        if (p.clc && lane == 0) {
+            bool in_flight = false;
+            for (int j = 0;; ++j) {
+                const int s = j % CLC_SLOTS;
+                const uint32_t round = (uint32_t)(j / CLC_SLOTS);
+                if (leader && j >= CLC_SLOTS && !wait_bar(cons_bar(s), (round - 1u) & 1u, p))
+                    break;
+                mbar_arrive_expect_tx(ready_bar(s), 16);
+                if (leader) {
+                    fence_proxy_async_smem();  // consumers' reads of the slot come first
+                    clc_try_cancel<CG == 2>(resp_addr(s), ready_bar(s));
+                }
+                in_flight = true;
+                if (!wait_bar(ready_bar(s), round & 1u, p)) break;
+                in_flight = false;
+                int x = 0;
+                if (!clc_query(resp_addr(s), &x)) break;
+            }
+            if (in_flight) grace_period_ns(200000);  // let a pending response land
+        }
         __syncwarp();
     }
 
@@ -623,7 +693,8 @@ int launch_variant(TcParams& tp, const DeviceInfo& dev, cudaStream_t stream) {
     }
     const int unit_rows = MC ? (tp.tiles_m + 1) / 2 : tp.tiles_m;
     const int total = unit_rows * tp.tiles_n;
-    int nclusters = max_clusters[dev.device & 63];
+    // persistent: as many clusters as fit at once; CLC: one cluster per tile
+    int nclusters = tp.clc ? total : max_clusters[dev.device & 63];
     if (nclusters > total) nclusters = total;
     if (nclusters < 1) nclusters = 1;
 
@@ -661,7 +732,7 @@ int dispatch_types(TcParams& tp, int dtype, bool a_mn, bool b_mn, const DeviceIn
 
 int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
                    uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled, int multicast,
-                   cudaStream_t stream) {
+                   int clc, cudaStream_t stream) {
     if (!get_encoder()) return kCuda;
     const int CG = cta_group == 1 ? 1 : 2;
     const bool mc = CG == 2 && multicast;
@@ -715,7 +786,8 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     tp.err = dev.err_word;
     tp.wait_limit_ns = wait_limit_ns;
     tp.fault_inject = fault_inject;
-    if ((int64_t)tp.tiles_m * tp.tiles_n > 0x7fffffffLL) return kUnsupported;
+    tp.clc = clc && !mc ? 1 : 0;  // the multicast variant keeps the static schedule
+    if ((int64_t)tp.tiles_m * tp.tiles_n * CG > 0x7fffffffLL) return kUnsupported;
 
     if (CG == 1)
         return dispatch_types<1, false>(tp, pr.dtype, !pr.a_kmajor, !pr.b_kmajor, dev, stream);

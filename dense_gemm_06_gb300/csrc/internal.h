@@ -68,9 +68,11 @@ int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd,
 // c_tma_enabled: 1 = store C with TMA when its rows are 16-byte aligned,
 // 0 = always use the st.global epilogue. multicast: 1 = clusters of two CTA
 // pairs sharing B through TMA multicast (2-CTA mode only).
+// clc: 1 = one cluster per tile, running clusters take over unstarted ones
+// with cluster launch control (try_cancel); 0 = persistent static schedule.
 int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, int cta_group,
                    uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled, int multicast,
-                   cudaStream_t stream);
+                   int clc, cudaStream_t stream);
 
 void note_launch(uint64_t n = 1);
 

@@ -154,6 +154,40 @@ __device__ __forceinline__ void st_async_v2_f32(uint32_t addr, float a, float b,
         :: "r"(addr), "f"(a), "f"(b), "r"(remote_bar) : "memory");
 }
 
+// ------------------------------------------------ cluster launch control --
+// Asks the hardware to cancel a cluster of this grid that has not started
+// yet; the 16-byte response lands at `resp` (16-byte aligned shared memory)
+// and completes 16 transaction bytes on `bar`. MULTICAST: the response goes to
+// the same offsets in every CTA of the cluster. After a response that reports
+// no cancellation, no further request may be issued.
+template <bool MULTICAST>
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    if constexpr (MULTICAST)
+        asm volatile(
+            "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+            ".multicast::cluster::all.b128 [%0], [%1];" :: "r"(resp), "r"(bar) : "memory");
+    else
+        asm volatile(
+            "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+            ".b128 [%0], [%1];" :: "r"(resp), "r"(bar) : "memory");
+}
+
+// Decodes a response: true if a cluster was cancelled, with the x index of
+// its first CTA in *ctaid_x (left 0 otherwise).
+__device__ __forceinline__ bool clc_query(uint32_t resp, int* ctaid_x) {
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "mov.u32 %1, 0;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(x) : "r"(resp) : "memory");
+    *ctaid_x = (int)x;
+    return ok != 0;
+}
+
 // 2-D tiled TMA store from this CTA's shared memory (bulk async-group).
 __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"

@@ -46,6 +46,10 @@ def main(argv=None):
     ap.add_argument("--cta-group", type=int, default=0)
     ap.add_argument("--simt-config", type=int, default=0)
     ap.add_argument("--tc-store", type=int, default=0)
+    ap.add_argument("--tc-scheduler", type=int, default=0,
+                    help="1 static persistent, 2 cluster launch control (0: automatic)")
+    ap.add_argument("--simt-split", type=int, default=0,
+                    help="FFMA last-wave K-split: 1 never, 2 always (0: automatic)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--tune", action="store_true",
                     help="run gemm_tune first (records the fastest configuration)")
@@ -71,6 +75,8 @@ def main(argv=None):
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_CTA_GROUP, a.cta_group))
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, a.simt_config))
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_STORE, a.tc_store))
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_SCHEDULER, a.tc_scheduler))
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, a.simt_split))
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
     if a.tune:

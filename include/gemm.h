@@ -205,6 +205,7 @@ typedef struct gemm_tuning {
     int tc_store;       /* 16-bit: 0 TMA store where possible, 1 st.global */
     float ms;           /* measured time per call of the chosen configuration */
     int candidates;     /* configurations measured */
+    int tc_scheduler;   /* 16-bit: 1 static persistent, 2 cluster launch control */
 } gemm_tuning;
 
 /*
@@ -326,7 +327,16 @@ enum gemm_option {
        epilogue), 1 = never split, 2 = always split the last wave (every tile
        when there is less than one wave). A split changes the order of the
        k-sum, never the per-product rounding. */
-    GEMM_OPT_SIMT_SPLIT_TAIL = 9
+    GEMM_OPT_SIMT_SPLIT_TAIL = 9,
+    /* Tile scheduler of the tensor-core kernel (the Gluon Multi-CTA
+       tutorial's CLC-scheduled matmul): 0 = automatic (currently static),
+       1 = static persistent (as many CTA pairs as fit, each walking every
+       n-th tile of the raster order), 2 = cluster launch control (one
+       cluster per tile is launched; running clusters take over tiles of
+       clusters that have not started with clusterlaunchcontrol.try_cancel,
+       a scheduler warp multicasting each response to both CTAs of the pair).
+       The operand-multicast variant always uses the static schedule. */
+    GEMM_OPT_TC_SCHEDULER = 10
 };
 
 /* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */

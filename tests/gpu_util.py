@@ -108,7 +108,7 @@ def make_operands(M, N, K, dtype, a_major, b_major, dist, seed, lda_pad=0, ldb_p
 
 
 def run_device_gemm(M, N, K, dtype, A, lda, a_major, B, ldb, b_major, c_major=1, ldc_pad=0,
-                    cta_group=0, dA=None, dB=None, tc_store=0, multicast=0):
+                    cta_group=0, dA=None, dB=None, tc_store=0, multicast=0, scheduler=0):
     """Runs gemm() through the C ABI; returns the logical C (float64)."""
     torch = torch_mod()
     ot = lg.OUT_TYPE[dtype]
@@ -121,9 +121,11 @@ def run_device_gemm(M, N, K, dtype, A, lda, a_major, B, ldb, b_major, c_major=1,
     old = lg.gemm_get_option(lg.GEMM_OPT_TC_CTA_GROUP)
     old_store = lg.gemm_get_option(lg.GEMM_OPT_TC_STORE)
     old_mc = lg.gemm_get_option(lg.GEMM_OPT_TC_MULTICAST)
+    old_sched = lg.gemm_get_option(lg.GEMM_OPT_TC_SCHEDULER)
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_CTA_GROUP, cta_group), "set_option")
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_STORE, tc_store), "set_option")
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_MULTICAST, multicast), "set_option")
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_SCHEDULER, scheduler), "set_option")
     try:
         rc = lg.gemm(M, N, K, dA if dA is not None else 0, lda, a_major,
                      dB if dB is not None else 0, ldb, b_major, cbuf.ptr(), ldc, c_major, dtype)
@@ -134,6 +136,7 @@ def run_device_gemm(M, N, K, dtype, A, lda, a_major, B, ldb, b_major, c_major=1,
         lg.gemm_set_option(lg.GEMM_OPT_TC_CTA_GROUP, old)
         lg.gemm_set_option(lg.GEMM_OPT_TC_STORE, old_store)
         lg.gemm_set_option(lg.GEMM_OPT_TC_MULTICAST, old_mc)
+        lg.gemm_set_option(lg.GEMM_OPT_TC_SCHEDULER, old_sched)
     return cbuf.read()
 
 

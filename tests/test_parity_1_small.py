@@ -37,17 +37,19 @@ def rne16(x: np.ndarray, t: str) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
-# tensor-core kernel modes: (CTA group, operand multicast across two pairs)
-TC_MODES = {"cg1": (1, 1), "cg2": (2, 1), "cg2mc": (2, 2)}
+# tensor-core kernel modes: (CTA group, operand multicast across two pairs,
+# tile scheduler: 1 static persistent, 2 cluster launch control)
+TC_MODES = {"cg1": (1, 1, 1), "cg2": (2, 1, 1), "cg2mc": (2, 2, 1), "cg1clc": (1, 1, 2),
+            "cg2clc": (2, 1, 2)}
 
 
 def run_and_check(M, N, K, dtype, am, bm, cm=1, dist="int", seed=0, lda_pad=0, ldb_pad=0,
-                  ldc_pad=0, cta_group=0, tc_store=0, multicast=0):
+                  ldc_pad=0, cta_group=0, tc_store=0, multicast=0, scheduler=0):
     A, lda, B, ldb = make_operands(M, N, K, dtype, am, bm, dist, seed, lda_pad, ldb_pad)
     C = run_device_gemm(M, N, K, dtype, A, lda, am, B, ldb, bm, cm, ldc_pad, cta_group,
-                        tc_store=tc_store, multicast=multicast)
+                        tc_store=tc_store, multicast=multicast, scheduler=scheduler)
     what = (f"{M}x{N}x{K} dtype={dtype} A{'KM'[am]} B{'KN'[bm]} C{'MN'[cm]} cg={cta_group} "
-            f"store={tc_store} mc={multicast}")
+            f"store={tc_store} mc={multicast} sched={scheduler}")
     ot = lg.OUT_TYPE[dtype]
     if dist == "int" and ot != "f32":
         import oracle
@@ -94,9 +96,9 @@ TC_SHAPES = [(1, 1, 1), (100, 70, 64), (300, 520, 200), (257, 513, 1037)]
 def test_tc_ragged_integer(shape, am, bm, dtype, mode, tc_store):
     # tc_store 0: TMA store of C where its rows are 16-byte aligned; 1: st.global
     M, N, K = shape
-    cg, mc = TC_MODES[mode]
+    cg, mc, sch = TC_MODES[mode]
     run_and_check(M, N, K, dtype, am, bm, 1, dist="int", seed=K, cta_group=cg,
-                  tc_store=tc_store, multicast=mc)
+                  tc_store=tc_store, multicast=mc, scheduler=sch)
 
 
 @pytest.mark.parametrize("tc_store", [0, 1])
@@ -104,9 +106,9 @@ def test_tc_ragged_integer(shape, am, bm, dtype, mode, tc_store):
 @pytest.mark.parametrize("dtype", TC_TYPES)
 @pytest.mark.parametrize("cm", [0, 1])
 def test_tc_normal_values(dtype, cm, mode, tc_store):
-    cg, mc = TC_MODES[mode]
+    cg, mc, sch = TC_MODES[mode]
     run_and_check(384, 520, 640, dtype, 0, 1, cm, dist="normal", seed=5, cta_group=cg,
-                  tc_store=tc_store, multicast=mc)
+                  tc_store=tc_store, multicast=mc, scheduler=sch)
 
 
 @pytest.mark.parametrize("mode", sorted(TC_MODES))
@@ -114,11 +116,11 @@ def test_tc_normal_values(dtype, cm, mode, tc_store):
 def test_tc_misaligned_leading_dims(am, bm, mode):
     # leading dimensions that are not 16-byte multiples force the repack path;
     # an odd ldc forces predicated scalar stores
-    cg, mc = TC_MODES[mode]
+    cg, mc, sch = TC_MODES[mode]
     run_and_check(333, 277, 131, lg.GEMM_F16_F32, am, bm, 1, dist="int", seed=6,
-                  lda_pad=1, ldb_pad=3, ldc_pad=1, cta_group=cg, multicast=mc)
+                  lda_pad=1, ldb_pad=3, ldc_pad=1, cta_group=cg, multicast=mc, scheduler=sch)
     run_and_check(333, 277, 131, lg.GEMM_BF16_BF16, am, bm, 0, dist="normal", seed=7,
-                  lda_pad=5, ldb_pad=1, ldc_pad=3, cta_group=cg, multicast=mc)
+                  lda_pad=5, ldb_pad=1, ldc_pad=3, cta_group=cg, multicast=mc, scheduler=sch)
 
 
 @pytest.mark.parametrize("mode", sorted(TC_MODES))
@@ -126,11 +128,11 @@ def test_tc_many_tiles_per_cta(mode):
     # more tiles than CTA pairs: exercises the TMEM double buffer and the
     # smem ring phases across tiles; an odd number of tile rows (11) leaves
     # the second pair of a multicast cluster without rows on the last units
-    cg, mc = TC_MODES[mode]
+    cg, mc, sch = TC_MODES[mode]
     run_and_check(2560, 2304, 320, lg.GEMM_F16_F32, 0, 0, 1, dist="int", seed=9,
-                  cta_group=cg, multicast=mc)
+                  cta_group=cg, multicast=mc, scheduler=sch)
     run_and_check(2816, 1280, 200, lg.GEMM_BF16_F32, 1, 1, 1, dist="int", seed=10,
-                  cta_group=cg, multicast=mc)
+                  cta_group=cg, multicast=mc, scheduler=sch)
 
 
 # ----------------------------------------------------- degenerate sizes --

@@ -75,26 +75,30 @@ def test_fp32_8192_cubed_all_majors(fp32_8192_logical, am, bm):
                   what=f"8192^3 fp32 A{'KM'[am]} B{'KN'[bm]}", seed=1027)
 
 
-@pytest.mark.parametrize("cta_group,multicast", [(0, 0), (1, 0), (2, 2)])
-def test_bf16_8192_cubed(cta_group, multicast):
+@pytest.mark.parametrize("cta_group,multicast,scheduler",
+                         [(0, 0, 0), (1, 0, 0), (2, 2, 0), (2, 1, 2), (1, 1, 2)])
+def test_bf16_8192_cubed(cta_group, multicast, scheduler):
     n = 8192
     A, lda, B, ldb = make_operands(n, n, n, lg.GEMM_BF16_BF16, 0, 0, "normal", 1028)
     C = run_device_gemm(n, n, n, lg.GEMM_BF16_BF16, A, lda, 0, B, ldb, 0, cta_group=cta_group,
-                        multicast=multicast)
+                        multicast=multicast, scheduler=scheduler)
     check_sampled(C, n, n, n, lg.GEMM_BF16_BF16, A, lda, 0, B, ldb, 0, exact=False,
-                  what=f"8192^3 bf16 (cg={cta_group}, mc={multicast})", seed=1028)
+                  what=f"8192^3 bf16 (cg={cta_group}, mc={multicast}, sched={scheduler})",
+                  seed=1028)
 
 
-def test_fp16_int_4095x3071x1037_ragged_bit_exact():
+@pytest.mark.parametrize("scheduler", [0, 2])
+def test_fp16_int_4095x3071x1037_ragged_bit_exact(scheduler):
     M, N, K = 4095, 3071, 1037
     A, lda, B, ldb = make_operands(M, N, K, lg.GEMM_F16_F32, 0, 1, "int", 1029, lo=-3, hi=3)
     assert (lda, ldb) == (1037, 3071)
-    C = run_device_gemm(M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1)
+    C = run_device_gemm(M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, scheduler=scheduler)
     check_full(C, M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, exact=True, what="4095x3071x1037 fp16 int")
 
 
-def test_fp16_int_16384x256x8192_skinny_bit_exact():
+@pytest.mark.parametrize("scheduler", [0, 2])
+def test_fp16_int_16384x256x8192_skinny_bit_exact(scheduler):
     M, N, K = 16384, 256, 8192
     A, lda, B, ldb = make_operands(M, N, K, lg.GEMM_F16_F32, 0, 1, "int", 1030, lo=-3, hi=3)
-    C = run_device_gemm(M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1)
+    C = run_device_gemm(M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, scheduler=scheduler)
     check_full(C, M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, exact=True, what="16384x256x8192 fp16 int")

@@ -27,8 +27,9 @@ def _lib():
     lg.load()
 
 
+@pytest.mark.parametrize("scheduler", [1, 2])
 @pytest.mark.parametrize("cta_group", [1, 2])
-def test_stalled_wait_times_out_and_device_recovers(cta_group):
+def test_stalled_wait_times_out_and_device_recovers(cta_group, scheduler):
     import torch
     n, k = 4096, 512  # >= 3 tiles per CTA pair: the MMA role also blocks
     dA = torch.zeros(n * k, dtype=torch.int16, device="cuda")
@@ -37,10 +38,12 @@ def test_stalled_wait_times_out_and_device_recovers(cta_group):
     assert lg.gemm_check_device_error() == lg.GEMM_OK
     saved = {o: lg.gemm_get_option(o) for o in (lg.GEMM_OPT_WAIT_LIMIT_NS,
                                                 lg.GEMM_OPT_TC_FAULT_INJECT,
-                                                lg.GEMM_OPT_TC_CTA_GROUP)}
+                                                lg.GEMM_OPT_TC_CTA_GROUP,
+                                                lg.GEMM_OPT_TC_SCHEDULER)}
     try:
         lg.check(lg.gemm_set_option(lg.GEMM_OPT_WAIT_LIMIT_NS, 20_000_000))
         lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_CTA_GROUP, cta_group))
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_SCHEDULER, scheduler))
         lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_FAULT_INJECT, 1))
         rc = lg.gemm(n, n, k, dA, k, 0, dB, k, 0, dC, n, 1, lg.GEMM_BF16_BF16)
         assert rc == lg.GEMM_OK  # asynchronous: the timeout is reported later
