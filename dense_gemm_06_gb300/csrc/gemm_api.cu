@@ -44,7 +44,7 @@ std::atomic<int> g_tc_multicast{0};
 // (no "automatic" values): an option set to a non-zero value wins, then a
 // gemm_tune() entry for the problem, then the built-in choice.
 struct RunConfig {
-    int simt_config;     // 1..6
+    int simt_config;     // 1..8
     int simt_transpose;  // 0 automatic size rule, 1 never, 2 always
     int cta_group;       // 1 or 2
     int multicast;       // 1 off, 2 on
@@ -357,7 +357,7 @@ RunConfig resolve(const TuneKey& key) {
             tuned = true;
         }
     }
-    if (c.simt_config == 0) c.simt_config = tuned && t.simt_config ? t.simt_config : 1;
+    if (c.simt_config == 0) c.simt_config = tuned && t.simt_config ? t.simt_config : 7;
     if (c.simt_transpose == 0 && tuned) c.simt_transpose = t.simt_transpose;
     if (c.cta_group == 0) c.cta_group = tuned && t.tc_cta_group ? t.tc_cta_group : 2;
     if (c.multicast == 0) c.multicast = tuned && t.tc_multicast ? t.tc_multicast : 1;
@@ -573,7 +573,7 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         int n = 0;
         if (dtype == GEMM_F32) {
             const bool any_kmajor = p.a_kmajor || p.b_kmajor;
-            for (int c = 1; c <= 6; ++c)
+            for (int c = 1; c <= 8; ++c)
                 for (int t = 1; t <= (any_kmajor ? 2 : 1); ++t) cands[n++] = {c, t, 2, 1, 0};
         } else {
             const bool c_aligned = aligned16_ld(C, ldc, out_bytes(dtype));
@@ -724,7 +724,7 @@ int gemm_set_option(int option, int64_t value) {
             g_fault_inject.store((int)value);
             return GEMM_OK;
         case GEMM_OPT_SIMT_CONFIG:
-            if (value < 0 || value > 6) return GEMM_ERR_INVALID_ARG;
+            if (value < 0 || value > 8) return GEMM_ERR_INVALID_ARG;
             g_simt_config.store((int)value);
             return GEMM_OK;
         case GEMM_OPT_SIMT_TRANSPOSE:

@@ -4,7 +4,10 @@
 // re-done by hand for sm_103a:
 //   * CTA tile 128 x 128 x BK, 256 threads, each thread owning an 8 x 8 block
 //     of C as four 4 x 4 quadrants (4 consecutive rows x 4 consecutive columns
-//     in each 64 x 64 sub-tile), so fragments load with 128-bit LDS;
+//     in each 64 x 64 sub-tile), so fragments load with 128-bit LDS; or 128
+//     threads owning 8 x 16 blocks (rows as above, columns in four groups of
+//     4 spaced 32 apart), which loads 24 fragment values per 128 FMAs
+//     instead of 16 per 64 and so needs a third fewer shared-memory reads;
 //   * A and B tiles always stored MN-major in shared memory (k-rows of 128
 //     floats, padded by 4 floats) so the fragment loads vectorise whatever
 //     the global major; a K-major operand is transposed on the way in with
@@ -35,21 +38,24 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int THREADS = 256;
 constexpr int PAD = 4;
 constexpr int LDS = BM + PAD;  // floats per k-row in shared memory (BM == BN)
 constexpr int BAND = 16;       // tile rows per raster band (L2 locality)
 
 static_assert(BM == BN, "one shared-memory row stride serves both operands");
 
-// Tile configurations (k-depth, ring depth, packed FMA, CTAs/SM). The CuTe Ampere
-// SGEMM example's default is 128 x 128 x 8 with 3 stages.
-template <int BK_, int STAGES_, bool FMA2_, int MINB_>
+// Tile configurations (k-depth, ring depth, packed FMA, CTAs/SM, columns per
+// thread). The CuTe Ampere SGEMM example's default is 128 x 128 x 8 with 3
+// stages (and 8 x 8 per thread).
+template <int BK_, int STAGES_, bool FMA2_, int MINB_, int TN_ = 8>
 struct SgCfg {
     static constexpr int BK = BK_;
     static constexpr int STAGES = STAGES_;
     static constexpr bool FMA2 = FMA2_;
     static constexpr int MINB = MINB_;  // CTAs per SM the register budget is sized for
+    static constexpr int TN = TN_;      // C columns per thread (8 or 16); rows: 8
+    static constexpr int THREADS = BM * BN / (8 * TN_);
+    static_assert(TN_ == 8 || TN_ == 16, "8 x 8 or 8 x 16 outputs per thread");
     static constexpr int OPERAND_FLOATS = BK * LDS;
     static constexpr int STAGE_FLOATS = 2 * OPERAND_FLOATS;
     static constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
@@ -68,7 +74,7 @@ struct SgemmParams {
     int dp_tiles;   // tiles 0 .. dp_tiles-1 (raster order) are computed whole
     int splits;     // K-slices of each later tile (one CTA per slice)
     int kt_slice;   // k-tiles per slice
-    float* ws;      // raw partial tiles of the slices: [unit][16][THREADS] float4
+    float* ws;      // raw partial tiles of the slices: [unit][BM * BN / 4] float4
 };
 
 // Raster: bands of BAND tile-rows, walking down M inside a band first.
@@ -82,27 +88,38 @@ __device__ __forceinline__ void tile_origin(const SgemmParams& p, int t, int& m0
     n0 = (within / rows_in_band) * BN;
 }
 
-// Thread -> C block: warp (wy, wx) = (w / 2, w % 2), lane (ly, lx) =
-// (l / 8, l % 8); ty in 0..15, tx in 0..15. The thread owns rows
-// ty*4 + (i & 3) + (i >> 2) * 64 and columns tx*4 + (c & 3) + (c >> 2) * 64.
+// Thread -> C block. A warp always spans 4 values of ty and 8 of tx (lane
+// (l / 8, l % 8)), so a fragment load reads 4 or 8 consecutive 16-byte units.
+// TN = 8: warp (wy, wx) = (w / 2, w % 2), ty in 0..15, tx in 0..15; the
+// thread owns rows ty*4 + (i & 3) + (i >> 2) * 64, columns
+// tx*4 + (c & 3) + (c >> 2) * 64. TN = 16: warp w covers ty = 4w .. 4w+3,
+// tx in 0..7; columns tx*4 + (c & 3) + (c >> 2) * 32.
+template <int TN>
 __device__ __forceinline__ void thread_block(int tid, int& ty, int& tx) {
     const int w = tid >> 5, l = tid & 31;
-    ty = (w >> 1) * 4 + (l >> 3);
-    tx = (w & 1) * 8 + (l & 7);
+    if constexpr (TN == 8) {
+        ty = (w >> 1) * 4 + (l >> 3);
+        tx = (w & 1) * 8 + (l & 7);
+    } else {
+        ty = w * 4 + (l >> 3);
+        tx = l & 7;
+    }
 }
 
-// Stores the thread's 8 x 8 block of the tile at (m0, n0), applying the fused
-// epilogue when one is active; predicated on M and N.
-__device__ __forceinline__ void store_block(const SgemmParams& p, const float2 (&acc)[8][4],
+// Stores the thread's 8 x TN block of the tile at (m0, n0), applying the
+// fused epilogue when one is active; predicated on M and N.
+template <int TN>
+__device__ __forceinline__ void store_block(const SgemmParams& p, const float2 (&acc)[8][TN / 2],
                                             int m0, int n0, int ty, int tx) {
+    constexpr int CSTRIDE = BN / (TN / 4);  // columns between a thread's 4-column groups
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = m0 + ty * 4 + (i & 3) + (i >> 2) * 64;
         if (row >= p.M) continue;
         float* crow = p.C + (int64_t)row * p.ldc;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int col = n0 + tx * 4 + h * 64;
+        for (int h = 0; h < TN / 4; ++h) {
+            const int col = n0 + tx * 4 + h * CSTRIDE;
             float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                           acc[i][2 * h + 1].y};
             if (p.epi.active) {  // D = act(alpha * acc + beta * C_old + bias)
@@ -160,12 +177,13 @@ __device__ __forceinline__ void cp_async_wait() {
 // laid out [k][r] with row stride LDS floats. Each thread keeps one pointer
 // that advances by one k-tile per call, a count of the k it has left and a
 // mask of its valid rows, so few registers stay live across the main loop.
-template <int BK, bool KMAJOR, int VEC>
+template <int BK, bool KMAJOR, int VEC, int T>
 struct TileLoader {
+    static constexpr int KROWS = T / 8;  // K-major: rows one pass covers (8 k each)
     const float* ptr;    // this thread's first element of the next k-tile
     int64_t ld;
     int k_left;          // K minus this thread's first k of the next tile
-    int rows_ok;         // K-major: bit q = row q*32 valid; MN 16B: valid rows of
+    int rows_ok;         // K-major: bit q = row q*KROWS valid; MN 16B: valid rows of
                          // the vector; MN 4B: 1 if the row is valid
     uint32_t s_off;      // byte offset of its first element inside a stage
 
@@ -175,16 +193,16 @@ struct TileLoader {
         ld = ld_;
         rows_ok = 0;
         if constexpr (KMAJOR) {
-            // element e = tid + 256 i: k-group h = e >> 10, row = (e & 1023) >> 3,
-            // k = 8 h + (e & 7); a thread's rows are (tid >> 3) + 32 q.
+            // element e = tid + T i: k-group h = e / 1024, row = (e % 1024) / 8,
+            // k = 8 h + e % 8; a thread's rows are tid / 8 + KROWS q.
             const int rr = tid >> 3, kk = tid & 7;
             ptr = X + (int64_t)(r0 + rr) * ld + k0 + kk;
             k_left = K - k0 - kk;
             s_off = (uint32_t)(kk * LDS + rr) * 4u;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) rows_ok |= (r0 + rr + 32 * q < R) << q;
+            for (int q = 0; q < BM / KROWS; ++q) rows_ok |= (r0 + rr + KROWS * q < R) << q;
         } else if constexpr (VEC == 4) {
-            // float4 idx = tid + 256 i: k = (tid >> 5) + 8 i, rows 4 (tid & 31) ..
+            // float4 idx = tid + T i: k = tid / 32 + (T / 32) i, rows 4 (tid % 32) ..
             const int rr = (tid & 31) << 2, kk = tid >> 5;
             ptr = X + (int64_t)(k0 + kk) * ld + r0 + rr;
             k_left = K - k0 - kk;
@@ -192,7 +210,7 @@ struct TileLoader {
             const int v = R - (r0 + rr);
             rows_ok = v >= 4 ? 4 : (v > 0 ? v : 0);
         } else {
-            // element e = tid + 256 i: k = (tid >> 7) + 2 i, row = tid & 127
+            // element e = tid + T i: k = tid / 128 + (T / 128) i, row = tid % 128
             const int rr = tid & 127, kk = tid >> 7;
             ptr = X + (int64_t)(k0 + kk) * ld + r0 + rr;
             k_left = K - k0 - kk;
@@ -204,31 +222,33 @@ struct TileLoader {
     // Issue the copies of the next k-tile into the stage at byte address s.
     __device__ __forceinline__ void load_next(uint32_t s) {
         if constexpr (KMAJOR) {
-            const int64_t ld32 = ld * 32;
+            const int64_t ldq = ld * KROWS;
 #pragma unroll
             for (int h = 0; h < BK / 8; ++h) {
                 const bool k_ok = 8 * h < k_left;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < BM / KROWS; ++q) {
                     const bool ok = k_ok && ((rows_ok >> q) & 1);
-                    cp_async_4(s + s_off + (uint32_t)(8 * h * LDS + 32 * q) * 4u,
-                               ptr + q * ld32 + 8 * h, ok);
+                    cp_async_4(s + s_off + (uint32_t)(8 * h * LDS + KROWS * q) * 4u,
+                               ptr + q * ldq + 8 * h, ok);
                 }
             }
             ptr += BK;
         } else if constexpr (VEC == 4) {
+            constexpr int KS = T / 32;  // k-rows one pass covers
 #pragma unroll
-            for (int i = 0; i < BK / 8; ++i) {
-                const bool ok = rows_ok > 0 && 8 * i < k_left;
-                cp_async_16(s + s_off + (uint32_t)(8 * i * LDS) * 4u, ptr + 8 * i * ld,
+            for (int i = 0; i < BK / KS; ++i) {
+                const bool ok = rows_ok > 0 && KS * i < k_left;
+                cp_async_16(s + s_off + (uint32_t)(KS * i * LDS) * 4u, ptr + KS * i * ld,
                             ok ? rows_ok * 4 : 0);
             }
             ptr += BK * ld;
         } else {
+            constexpr int KS = T / 128;
 #pragma unroll
-            for (int i = 0; i < BK / 2; ++i) {
-                const bool ok = rows_ok && 2 * i < k_left;
-                cp_async_4(s + s_off + (uint32_t)(2 * i * LDS) * 4u, ptr + 2 * i * ld, ok);
+            for (int i = 0; i < BK / KS; ++i) {
+                const bool ok = rows_ok && KS * i < k_left;
+                cp_async_4(s + s_off + (uint32_t)(KS * i * LDS) * 4u, ptr + KS * i * ld, ok);
             }
             ptr += BK * ld;
         }
@@ -237,9 +257,13 @@ struct TileLoader {
 };
 
 template <class Cfg, bool A_K, int A_VEC, bool B_K, int B_VEC>
-__global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const SgemmParams p) {
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) sgemm_ffma_kernel(const SgemmParams p) {
     constexpr int BK = Cfg::BK;
     constexpr int STAGES = Cfg::STAGES;
+    constexpr int T = Cfg::THREADS;
+    constexpr int TN = Cfg::TN;
+    constexpr int NB = TN / 4;           // 4-column groups per thread
+    constexpr int CSTEP = BN / NB / 4;   // float4s between a thread's groups
     extern __shared__ __align__(16) float smem[];
     const int tid = threadIdx.x;
 
@@ -254,12 +278,12 @@ __global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const Sg
     }
     int m0, n0, ty, tx;
     tile_origin(p, t, m0, n0);
-    thread_block(tid, ty, tx);
+    thread_block<TN>(tid, ty, tx);
 
     const uint32_t s0 = smem_addr(smem);
 
-    TileLoader<BK, A_K, A_VEC> la;
-    TileLoader<BK, B_K, B_VEC> lb;
+    TileLoader<BK, A_K, A_VEC, T> la;
+    TileLoader<BK, B_K, B_VEC, T> lb;
     la.init(p.A, p.lda, p.M, p.K, m0, kt0 * BK, tid);
     lb.init(p.B, p.ldb, p.N, p.K, n0, kt0 * BK, tid);
     // Tiles are issued strictly in order kt = 0, 1, 2, ...
@@ -278,11 +302,11 @@ __global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const Sg
     // acc[i][jj] holds the C columns (2 jj, 2 jj + 1) of b-index space of
     // row i: packed pairs for the two-lane FMA (fma.rn.f32x2 on sm_100+), or
     // two scalar FMAs; both round each product-sum once (IEEE fma).
-    float2 acc[8][4];
+    float2 acc[8][TN / 2];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
+        for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
     for (int kt = 0; kt < nkt; ++kt) {
         cp_async_wait<STAGES - 2>();
@@ -298,19 +322,24 @@ __global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const Sg
         // Fully unrolled over the tile's k: the compiler hoists the 128-bit
         // fragment loads of step k+1 above the FMAs of step k as registers
         // allow (an explicit second fragment buffer does not fit next to
-        // the 64 accumulators at 2 CTAs/SM).
+        // the accumulators).
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
             const float4* pa = reinterpret_cast<const float4*>(sA + k * LDS + ty * 4);
             const float4* pb = reinterpret_cast<const float4*>(sB + k * LDS + tx * 4);
-            const float4 a0 = pa[0], a1 = pa[16], b0 = pb[0], b1 = pb[16];
+            const float4 a0 = pa[0], a1 = pa[16];
             const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float2 b[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                 make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+            float2 b[TN / 2];
+#pragma unroll
+            for (int g = 0; g < NB; ++g) {
+                const float4 q = pb[g * CSTEP];
+                b[2 * g] = make_float2(q.x, q.y);
+                b[2 * g + 1] = make_float2(q.z, q.w);
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < TN / 2; ++j) {
                     if constexpr (Cfg::FMA2) {
                         acc[i][j] = __ffma2_rn(make_float2(a[i], a[i]), b[j], acc[i][j]);
                     } else {
@@ -325,50 +354,55 @@ __global__ void __launch_bounds__(THREADS, Cfg::MINB) sgemm_ffma_kernel(const Sg
 
     if ((int)blockIdx.x >= p.dp_tiles) {  // a K-slice of a tail tile: raw partial sums
         const int unit = (int)blockIdx.x - p.dp_tiles;
-        float4* wsp = reinterpret_cast<float4*>(p.ws) + (size_t)unit * (16 * THREADS) + tid;
+        float4* wsp = reinterpret_cast<float4*>(p.ws) + (size_t)unit * (BM * BN / 4) + tid;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                wsp[(2 * i + h) * THREADS] = make_float4(acc[i][2 * h].x, acc[i][2 * h].y,
-                                                         acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+            for (int h = 0; h < NB; ++h)
+                wsp[(NB * i + h) * T] = make_float4(acc[i][2 * h].x, acc[i][2 * h].y,
+                                                    acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
         return;
     }
-    store_block(p, acc, m0, n0, ty, tx);
+    store_block<TN>(p, acc, m0, n0, ty, tx);
 }
 
 // Tail fixup: tile dp_tiles + blockIdx.x = the sum of its K-slices' partial
-// tiles, added in slice order, then the normal epilogue.
-__global__ void __launch_bounds__(THREADS) sgemm_split_fixup_kernel(const SgemmParams p) {
+// tiles, added in slice order, then the normal epilogue (same thread -> C
+// mapping as the main kernel of this TN).
+template <int TN>
+__global__ void __launch_bounds__(BM * BN / (8 * TN)) sgemm_split_fixup_kernel(
+    const SgemmParams p) {
+    constexpr int T = BM * BN / (8 * TN);
+    constexpr int NB = TN / 4;
     const int tid = threadIdx.x;
     int m0, n0, ty, tx;
     tile_origin(p, p.dp_tiles + blockIdx.x, m0, n0);
-    thread_block(tid, ty, tx);
+    thread_block<TN>(tid, ty, tx);
     const float4* wsp = reinterpret_cast<const float4*>(p.ws) +
-                        (size_t)blockIdx.x * p.splits * (16 * THREADS) + tid;
-    float2 acc[8][4];
+                        (size_t)blockIdx.x * p.splits * (BM * BN / 4) + tid;
+    float2 acc[8][TN / 2];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float4 q = wsp[(2 * i + h) * THREADS];
+        for (int h = 0; h < NB; ++h) {
+            const float4 q = wsp[(NB * i + h) * T];
             acc[i][2 * h] = make_float2(q.x, q.y);
             acc[i][2 * h + 1] = make_float2(q.z, q.w);
         }
     for (int sl = 1; sl < p.splits; ++sl) {
-        const float4* w = wsp + (size_t)sl * (16 * THREADS);
+        const float4* w = wsp + (size_t)sl * (BM * BN / 4);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float4 q = w[(2 * i + h) * THREADS];
+            for (int h = 0; h < NB; ++h) {
+                const float4 q = w[(NB * i + h) * T];
                 acc[i][2 * h].x += q.x;
                 acc[i][2 * h].y += q.y;
                 acc[i][2 * h + 1].x += q.z;
                 acc[i][2 * h + 1].y += q.w;
             }
     }
-    store_block(p, acc, m0, n0, ty, tx);
+    store_block<TN>(p, acc, m0, n0, ty, tx);
 }
 
 // Sets the dynamic shared-memory limit of `kern` once per device; `done` is
@@ -424,7 +458,7 @@ int launch_variant(SgemmParams sp, int device, int sm_count, int split_mode, Scr
     if (!configure_once(kern, configured, device, Cfg::SMEM_BYTES)) return kCuda;
     int occ = per_sm[device & 63].load();
     if (occ == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::THREADS,
                                                           Cfg::SMEM_BYTES) != cudaSuccess) {
             cudaGetLastError();
             occ = -1;
@@ -442,12 +476,13 @@ int launch_variant(SgemmParams sp, int device, int sm_count, int split_mode, Scr
         }
     }
     const int64_t units = sp.dp_tiles + ((int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles) * sp.splits;
-    kern<<<dim3((unsigned)units), dim3(THREADS), Cfg::SMEM_BYTES, stream>>>(sp);
+    kern<<<dim3((unsigned)units), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream>>>(sp);
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     note_launch();
     const int64_t fix = (int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles;
     if (fix > 0) {
-        sgemm_split_fixup_kernel<<<dim3((unsigned)fix), dim3(THREADS), 0, stream>>>(sp);
+        sgemm_split_fixup_kernel<Cfg::TN>
+            <<<dim3((unsigned)fix), dim3(Cfg::THREADS), 0, stream>>>(sp);
         if (cudaGetLastError() != cudaSuccess) return kCuda;
         note_launch();
     }
@@ -552,6 +587,8 @@ int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, int s
         case 4: return launch_layout<SgCfg<8, 3, true, 2>>(sp, av, bv, d, n, split_mode, scratch, stream);
         case 5: return launch_layout<SgCfg<16, 4, true, 1>>(sp, av, bv, d, n, split_mode, scratch, stream);
         case 6: return launch_layout<SgCfg<32, 4, true, 1>>(sp, av, bv, d, n, split_mode, scratch, stream);
+        case 7: return launch_layout<SgCfg<16, 4, true, 2, 16>>(sp, av, bv, d, n, split_mode, scratch, stream);
+        case 8: return launch_layout<SgCfg<32, 3, true, 2, 16>>(sp, av, bv, d, n, split_mode, scratch, stream);
         default: return launch_layout<SgCfg<16, 4, true, 2>>(sp, av, bv, d, n, split_mode, scratch, stream);
     }
 }

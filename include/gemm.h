@@ -289,14 +289,18 @@ enum gemm_option {
        out (after GEMM_OPT_WAIT_LIMIT_NS) and reports GEMM_ERR_TIMEOUT through
        gemm_check_device_error. 0 (default) = off. */
     GEMM_OPT_TC_FAULT_INJECT = 3,
-    /* Tile configuration of the fp32 FFMA kernel (all 128 x 128 CTA tiles,
-       256 threads, 8 x 8 outputs per thread), as (k-depth, ring stages,
-       FMA form, CTAs per SM the registers are sized for): 0 = automatic,
-       1 = (16, 4, packed, 2), 2 = (16, 4, scalar, 2), 3 = (32, 3, packed, 2),
-       4 = (8, 3, packed, 2) -- the CuTe Ampere example's 128 x 128 x 8 with
-       3 stages --, 5 = (16, 4, packed, 1), 6 = (32, 4, packed, 1). "Packed"
-       is the two-lane fma.rn.f32x2. Every configuration rounds each
-       multiply-add once (IEEE fma) and sums k in the same order. */
+    /* Tile configuration of the fp32 FFMA kernel (all 128 x 128 CTA tiles),
+       as (k-depth, ring stages, FMA form, CTAs per SM the registers are
+       sized for, outputs per thread): 0 = automatic (7, the fastest
+       measured at 8192^3),
+       1 = (16, 4, packed, 2, 8 x 8), 2 = (16, 4, scalar, 2, 8 x 8),
+       3 = (32, 3, packed, 2, 8 x 8), 4 = (8, 3, packed, 2, 8 x 8) -- the CuTe
+       Ampere example's 128 x 128 x 8 with 3 stages --,
+       5 = (16, 4, packed, 1, 8 x 8), 6 = (32, 4, packed, 1, 8 x 8),
+       7 = (16, 4, packed, 2, 8 x 16), 8 = (32, 3, packed, 2, 8 x 16).
+       8 x 8 runs 256 threads per CTA, 8 x 16 runs 128. "Packed" is the
+       two-lane fma.rn.f32x2. Every configuration rounds each multiply-add
+       once (IEEE fma) and sums k in the same order. */
     GEMM_OPT_SIMT_CONFIG = 4,
     /* K-major fp32 operands: 0 = automatic (an operand is first transposed
        into an MN-major copy in pool scratch when the other output dimension

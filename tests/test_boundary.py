@@ -147,8 +147,8 @@ def test_strerror_and_options(lib):
     assert lg.gemm_get_option(lg.GEMM_OPT_TC_CTA_GROUP) == 0
     assert lg.gemm_get_option(lg.GEMM_OPT_TC_FAULT_INJECT) == 0
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_CONFIG) == 0
-    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 7) == lg.GEMM_ERR_INVALID_ARG
-    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 6) == 0
+    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 9) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 8) == 0
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 0) == 0
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_TRANSPOSE) == 0
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_TRANSPOSE, 3) == lg.GEMM_ERR_INVALID_ARG

@@ -160,7 +160,7 @@ def test_k_one(dtype):
     run_and_check(129, 257, 1, dtype, 1, 0, 1, dist="int", seed=2)
 
 
-@pytest.mark.parametrize("config", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("config", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("am,bm", list(itertools.product((0, 1), (0, 1))))
 def test_sgemm_every_tile_config(config, am, bm):
     old = lg.gemm_get_option(lg.GEMM_OPT_SIMT_CONFIG)
@@ -189,7 +189,7 @@ def test_sgemm_with_and_without_operand_transpose(transpose, am, bm, cm):
 # K-split of the FFMA kernel's last wave (GEMM_OPT_SIMT_SPLIT_TAIL): forced on
 # small and ragged shapes (every tile split, slices of one k-tile or empty),
 # and the automatic rule on a shape whose last wave is nearly empty.
-@pytest.mark.parametrize("config", [1, 5])
+@pytest.mark.parametrize("config", [1, 5, 7])
 @pytest.mark.parametrize("am,bm,cm", list(itertools.product((0, 1), (0, 1), (0, 1))))
 def test_sgemm_split_tail_forced(config, am, bm, cm):
     old = {o: lg.gemm_get_option(o) for o in (lg.GEMM_OPT_SIMT_SPLIT_TAIL,
