@@ -509,6 +509,13 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         const size_t a_bytes = (size_t)(a_outer * lda_d * ie), b_bytes = (size_t)(b_outer * ldb_d * ie);
         const size_t c_bytes = (size_t)(c_outer * ldc_d * oe);
 
+        // One flat copy when both sides are packed rows, else a pitched copy.
+        auto copy = [&](void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
+                        size_t height, cudaMemcpyKind kind) {
+            if (dpitch == width && spitch == width)
+                return cudaMemcpyAsync(dst, src, width * height, kind, s);
+            return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind, s);
+        };
         void *dA = nullptr, *dB = nullptr, *dC = nullptr;
         auto release = [&] {
             if (dA) cudaFreeAsync(dA, s);
@@ -523,10 +530,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
             return kCuda;
         }
         if (K > 0) {
-            if (cudaMemcpy2DAsync(dA, lda_d * ie, A, lda * ie, a_inner * ie, a_outer,
-                                  cudaMemcpyHostToDevice, s) != cudaSuccess ||
-                cudaMemcpy2DAsync(dB, ldb_d * ie, B, ldb * ie, b_inner * ie, b_outer,
-                                  cudaMemcpyHostToDevice, s) != cudaSuccess) {
+            if (copy(dA, lda_d * ie, A, lda * ie, a_inner * ie, a_outer,
+                     cudaMemcpyHostToDevice) != cudaSuccess ||
+                copy(dB, ldb_d * ie, B, ldb * ie, b_inner * ie, b_outer,
+                     cudaMemcpyHostToDevice) != cudaSuccess) {
                 cudaGetLastError();
                 release();
                 return kCuda;
@@ -538,8 +545,8 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
                                                dC, ldc_d, c_major, dtype));
         rc = run_device(p, *dev, pool, cfg, s);
         if (rc == kOk &&
-            cudaMemcpy2DAsync(C, ldc * oe, dC, ldc_d * oe, c_inner * oe, c_outer,
-                              cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+            copy(C, ldc * oe, dC, ldc_d * oe, c_inner * oe, c_outer,
+                 cudaMemcpyDeviceToHost) != cudaSuccess) {
             cudaGetLastError();
             rc = kCuda;
         }
