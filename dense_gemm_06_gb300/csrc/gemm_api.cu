@@ -9,10 +9,12 @@
 // layout.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <numeric>
 #include <mutex>
 
 #include "../../include/gemm.h"
@@ -77,6 +79,7 @@ struct DeviceState {
     int status = kOk;
     DeviceInfo info{};
     cudaMemPool_t pool = nullptr;
+    cudaStream_t h2d = nullptr, d2h = nullptr;  // gemm_host's copy streams
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -128,12 +131,24 @@ int current_device(DeviceInfo** out, cudaMemPool_t* pool) {
         st.info.cc_major = prop.major;
         st.info.cc_minor = prop.minor;
         st.info.err_word = static_cast<unsigned int*>(err);
+        if (cudaStreamCreateWithFlags(&st.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&st.d2h, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            st.status = kCuda;
+            return;
+        }
         st.status = kOk;
     });
     if (st.status != kOk) return st.status;
     *out = &st.info;
     if (pool) *pool = st.pool;
     return kOk;
+}
+
+// gemm_host's copy streams of the current device (after current_device()).
+void copy_streams(const DeviceInfo& dev, cudaStream_t* h2d, cudaStream_t* d2h) {
+    *h2d = g_dev[dev.device].h2d;
+    *d2h = g_dev[dev.device].d2h;
 }
 
 bool mul_fits(int64_t a, int64_t b, int64_t limit) { return a == 0 || b <= limit / a; }
@@ -485,6 +500,30 @@ int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_m
     }
 }
 
+namespace {
+
+// Rows of the normalised C per gemm_host panel: a whole number of waves of
+// the kernel that computes it (so no panel adds a partial wave), at most
+// about 8 panels; M itself when the product is too small for overlapping the
+// copies with compute to pay.
+int64_t host_panel_rows(const Problem& p, const DeviceInfo& dev, const RunConfig& cfg) {
+    if (p.K == 0 || (double)p.M * (double)p.N * (double)p.K < 1.0e10) return p.M;
+    const bool f32 = p.dtype == GEMM_F32;
+    const bool one_cta = f32 || cfg.cta_group == 1;
+    const int64_t tm = f32 ? 128 : (cfg.cta_group == 1 ? 128 : (cfg.multicast == 2 ? 512 : 256));
+    const int64_t tn = f32 ? 128 : 256;
+    int64_t slots = f32 ? (int64_t)dev.sm_count * (cfg.simt_config == 5 || cfg.simt_config == 6
+                                                      ? 1 : 2)
+                        : (int64_t)dev.sm_count / (one_cta ? 1 : (cfg.multicast == 2 ? 4 : 2));
+    if (slots < 1) slots = 1;
+    const int64_t tiles_m = (p.M + tm - 1) / tm, tiles_n = (p.N + tn - 1) / tn;
+    int64_t r = slots / std::gcd(slots, tiles_n);
+    while (r * 8 < tiles_m) r *= 2;
+    return r >= tiles_m ? p.M : r * tm;
+}
+
+}  // namespace
+
 int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
               const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
               int dtype, void* stream) {
@@ -497,6 +536,8 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         rc = current_device(&dev, &pool);
         if (rc != kOk) return rc;
         cudaStream_t s = static_cast<cudaStream_t>(stream);
+        cudaStream_t h2d = nullptr, d2h = nullptr;
+        copy_streams(*dev, &h2d, &d2h);
         const int ie = in_bytes(dtype), oe = out_bytes(dtype);
 
         // Device copies with 16-byte aligned row pitches.
@@ -510,47 +551,108 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         const size_t c_bytes = (size_t)(c_outer * ldc_d * oe);
 
         // One flat copy when both sides are packed rows, else a pitched copy.
-        auto copy = [&](void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
-                        size_t height, cudaMemcpyKind kind) {
+        auto copy = [](void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
+                       size_t height, cudaMemcpyKind kind, cudaStream_t st) {
             if (dpitch == width && spitch == width)
-                return cudaMemcpyAsync(dst, src, width * height, kind, s);
-            return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind, s);
+                return cudaMemcpyAsync(dst, src, width * height, kind, st);
+            return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind, st);
         };
         void *dA = nullptr, *dB = nullptr, *dC = nullptr;
-        auto release = [&] {
-            if (dA) cudaFreeAsync(dA, s);
-            if (dB) cudaFreeAsync(dB, s);
-            if (dC) cudaFreeAsync(dC, s);
-        };
         if (cudaMallocFromPoolAsync(&dC, c_bytes, pool, s) != cudaSuccess ||
             (K > 0 && (cudaMallocFromPoolAsync(&dA, a_bytes, pool, s) != cudaSuccess ||
                        cudaMallocFromPoolAsync(&dB, b_bytes, pool, s) != cudaSuccess))) {
             cudaGetLastError();
-            release();
+            if (dA) cudaFreeAsync(dA, s);
+            if (dB) cudaFreeAsync(dB, s);
+            if (dC) cudaFreeAsync(dC, s);
             return kCuda;
         }
-        if (K > 0) {
-            if (copy(dA, lda_d * ie, A, lda * ie, a_inner * ie, a_outer,
-                     cudaMemcpyHostToDevice) != cudaSuccess ||
-                copy(dB, ldb_d * ie, B, ldb * ie, b_inner * ie, b_outer,
-                     cudaMemcpyHostToDevice) != cudaSuccess) {
-                cudaGetLastError();
-                release();
-                return kCuda;
-            }
-        }
-        const Problem p = normalise(M, N, K, dA, lda_d, a_major, dB, ldb_d, b_major, dC, ldc_d,
-                                    c_major, dtype);
+        // The same normalisation (C column-major: the transposed problem) of
+        // the host and the device views; panels run over its rows.
+        const Problem ph = normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major,
+                                     dtype);
+        const Problem pd = normalise(M, N, K, dA, lda_d, a_major, dB, ldb_d, b_major, dC, ldc_d,
+                                     c_major, dtype);
         const RunConfig cfg = resolve(make_key(M, N, K, dA, lda_d, a_major, dB, ldb_d, b_major,
                                                dC, ldc_d, c_major, dtype));
-        rc = run_device(p, *dev, pool, cfg, s);
-        if (rc == kOk &&
-            copy(C, ldc * oe, dC, ldc_d * oe, c_inner * oe, c_outer,
-                 cudaMemcpyDeviceToHost) != cudaSuccess) {
+        const int64_t rows = host_panel_rows(pd, *dev, cfg);
+        const int panels = (int)((pd.M + rows - 1) / rows);
+
+        // Events: allocation done (s), B (and A unless it goes by panels)
+        // in, each A panel in, each C panel computed, both copy streams done.
+        constexpr int kMaxPanels = 64;
+        cudaEvent_t ev[2 * kMaxPanels + 4] = {};
+        int nev = 0;
+        auto event = [&]() -> cudaEvent_t {
+            cudaEvent_t e = nullptr;
+            if (nev < 2 * kMaxPanels + 4 &&
+                cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess) {
+                ev[nev++] = e;
+                return e;
+            }
             cudaGetLastError();
-            rc = kCuda;
+            return nullptr;
+        };
+        auto ok = [&](cudaError_t e) {
+            if (e != cudaSuccess && rc == kOk) rc = kCuda;
+            return rc == kOk;
+        };
+        // A panel of A's rows is one copy of contiguous rows when A (in the
+        // normalised problem) is K-major; otherwise A goes in whole with B.
+        const bool a_panels = panels > 1 && pd.a_kmajor && panels <= kMaxPanels;
+        const int np = a_panels || panels <= kMaxPanels ? panels : 1;
+        const int64_t prow = np == 1 ? pd.M : rows;
+        cudaEvent_t e_alloc = event(), e_b = event();
+        if (!e_alloc || !e_b) rc = kCuda;
+        if (ok(cudaEventRecord(e_alloc, s)) && ok(cudaStreamWaitEvent(h2d, e_alloc, 0)) && K > 0) {
+            const char* hB = static_cast<const char*>(ph.B);
+            char* dBp = static_cast<char*>(const_cast<void*>(pd.B));
+            const int64_t bi = pd.b_kmajor ? K : pd.N, bo = pd.b_kmajor ? pd.N : K;
+            ok(copy(dBp, pd.ldb * ie, hB, ph.ldb * ie, bi * ie, bo, cudaMemcpyHostToDevice, h2d));
+            if (!a_panels) {
+                const int64_t ai = pd.a_kmajor ? K : pd.M, ao = pd.a_kmajor ? pd.M : K;
+                ok(copy(const_cast<void*>(pd.A), pd.lda * ie, ph.A, ph.lda * ie, ai * ie, ao,
+                        cudaMemcpyHostToDevice, h2d));
+            }
         }
-        release();
+        if (rc == kOk) ok(cudaEventRecord(e_b, h2d));
+        if (rc == kOk) ok(cudaStreamWaitEvent(s, e_b, 0));
+        for (int i = 0; i < np && rc == kOk; ++i) {
+            const int64_t m0 = i * prow, m1 = std::min<int64_t>(pd.M, m0 + prow);
+            Problem q = pd;
+            q.M = m1 - m0;
+            q.C = static_cast<char*>(pd.C) + m0 * pd.ldc * oe;
+            if (K > 0) q.A = static_cast<const char*>(pd.A) + (pd.a_kmajor ? m0 * pd.lda : m0) * ie;
+            if (a_panels && K > 0) {
+                cudaEvent_t e_a = event();
+                if (!e_a) { rc = kCuda; break; }
+                ok(copy(const_cast<void*>(q.A), pd.lda * ie,
+                        static_cast<const char*>(ph.A) + m0 * ph.lda * ie, ph.lda * ie, K * ie,
+                        q.M, cudaMemcpyHostToDevice, h2d));
+                if (rc == kOk) ok(cudaEventRecord(e_a, h2d));
+                if (rc == kOk) ok(cudaStreamWaitEvent(s, e_a, 0));
+            }
+            if (rc == kOk) rc = run_device(q, *dev, pool, cfg, s);
+            cudaEvent_t e_c = rc == kOk ? event() : nullptr;
+            if (rc == kOk && !e_c) rc = kCuda;
+            if (rc == kOk) ok(cudaEventRecord(e_c, s));
+            if (rc == kOk) ok(cudaStreamWaitEvent(d2h, e_c, 0));
+            if (rc == kOk)
+                ok(copy(static_cast<char*>(ph.C) + m0 * ph.ldc * oe, ph.ldc * oe, q.C,
+                        pd.ldc * oe, pd.N * oe, q.M, cudaMemcpyDeviceToHost, d2h));
+        }
+        // Whatever was enqueued on the copy streams finishes before the
+        // caller's stream goes on (and before the scratch is freed).
+        cudaEvent_t e_in = event(), e_out = event();
+        if (e_in && cudaEventRecord(e_in, h2d) == cudaSuccess) cudaStreamWaitEvent(s, e_in, 0);
+        else rc = rc == kOk ? kCuda : rc;
+        if (e_out && cudaEventRecord(e_out, d2h) == cudaSuccess) cudaStreamWaitEvent(s, e_out, 0);
+        else rc = rc == kOk ? kCuda : rc;
+        cudaGetLastError();
+        if (dA) cudaFreeAsync(dA, s);
+        if (dB) cudaFreeAsync(dB, s);
+        cudaFreeAsync(dC, s);
+        for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);
         return rc;
     } catch (...) {
         return kCuda;
