@@ -379,6 +379,9 @@ def profiled_traffic(kernel: str):
 # ------------------------------------------------------ CPU baselines --
 
 CPU_ROWS = 400  # rows of each 8192^3 GEMM the oracle computes per sample (~10 s)
+# Reference arm: rows per timed step (~5 s on 16 host cores, so 10 steps plus
+# warm-up take about a minute; fewer rows would mostly time the decoding of B)
+REF_ROWS = 256
 
 
 def oracle_sample(f32, bf, rows_per_gemm):
@@ -415,7 +418,7 @@ def run_reference(args):
         return
     import oracle
     f32, bf = make_inputs()
-    rows = 16
+    rows = REF_ROWS
     for _ in range(args.warmup):
         oracle_sample(f32, bf, 2)
     tot_flops, tot_s = 0.0, 0.0
