@@ -27,7 +27,16 @@ import pytest
 
 import datagen
 import dense_gemm_06_gb300 as lg
-from gpu_util import check_full, check_sampled, make_operands, run_device_gemm
+import oracle
+from gpu_util import check_full, check_sampled, decode, make_operands, run_device_gemm, to_device
+
+
+def rne16(x: np.ndarray, t: str) -> np.ndarray:
+    """Round exact (integer-valued) results to the 16-bit output type."""
+    if t == "f16":
+        return x.astype(np.float16).astype(np.float64)
+    bits = datagen.f32_to_bf16_bits(x.astype(np.float32))
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 pytestmark = pytest.mark.gpu
 
@@ -102,3 +111,52 @@ def test_fp16_int_16384x256x8192_skinny_bit_exact(scheduler):
     A, lda, B, ldb = make_operands(M, N, K, lg.GEMM_F16_F32, 0, 1, "int", 1030, lo=-3, hi=3)
     C = run_device_gemm(M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, scheduler=scheduler)
     check_full(C, M, N, K, lg.GEMM_F16_F32, A, lda, 0, B, ldb, 1, exact=True, what="16384x256x8192 fp16 int")
+
+
+@pytest.mark.parametrize("dtype,am,bm,cm", [(lg.GEMM_F32, 0, 1, 1), (lg.GEMM_BF16_BF16, 0, 0, 0)])
+def test_c_beyond_4g_elements(dtype, am, bm, cm):
+    # C with 70001 x 65537 > 2^32 elements (18.4 GB in fp32): every row offset
+    # past 2^32 elements must be formed in 64 bits. Guard bands of 64 elements
+    # on both sides of C must stay untouched; rows and columns are sampled
+    # (the first and last included) and compared bit-exactly.
+    import torch
+    M, N, K = 70001, 65537, 40
+    ot = lg.OUT_TYPE[dtype]
+    A, lda, B, ldb = make_operands(M, N, K, dtype, am, bm, "int", 1040, lo=-3, hi=3)
+    ldc = N if cm == 1 else M
+    outer = M if cm == 1 else N
+    tdt = torch.float32 if ot == "f32" else torch.int16
+    canary = float("nan") if ot == "f32" else 0x7FDA
+    dC = torch.full((outer * ldc + 128,), canary, dtype=tdt, device="cuda")
+    esz = 4 if ot == "f32" else 2
+    lg.check(lg.gemm(M, N, K, to_device(A), lda, am, to_device(B), ldb, bm,
+                     int(dC.data_ptr()) + 64 * esz, ldc, cm, dtype), "gemm")
+    lg.check(lg.gemm_check_device_error(), "device error word")
+    torch.cuda.synchronize()
+    guard = torch.cat([dC[:64], dC[-64:]]).cpu().numpy()
+    if ot == "f32":
+        assert np.all(np.isnan(guard)), "guard band written"
+    else:
+        assert np.all(guard.view(np.uint16) == 0x7FDA), "guard band written"
+    body = dC[64:64 + outer * ldc].view(outer, ldc)
+    it = lg.IN_TYPE[dtype]
+    rows = datagen.sample_indices(M, 48, seed=1041, stream=101)
+    cols = datagen.sample_indices(N, 48, seed=1041, stream=102)
+
+    def logical(block):  # device block of storage -> logical float64
+        raw = block.cpu().numpy()
+        return decode(raw.view(np.float32) if ot == "f32" else raw.view(np.uint16), ot)
+
+    if cm == 1:
+        Cr = logical(body[torch.as_tensor(rows, device="cuda")])
+        Cc = logical(body[:, torch.as_tensor(cols, device="cuda")])
+    else:
+        Cr = logical(body[:, torch.as_tensor(rows, device="cuda")]).T
+        Cc = logical(body[torch.as_tensor(cols, device="cuda")]).T
+    R, _ = oracle.gemm_ref(M, N, K, A, lda, am, it, B, ldb, bm, it, rows=rows)
+    Cl, _ = oracle.gemm_ref(M, N, K, A, lda, am, it, B, ldb, bm, it, cols=cols)
+    want_r, want_c = (R, Cl) if ot == "f32" else (rne16(R, ot), rne16(Cl, ot))
+    assert np.array_equal(Cr, want_r), "sampled rows"
+    assert np.array_equal(Cc, want_c), "sampled columns"
+    del dC, body
+    torch.cuda.empty_cache()
