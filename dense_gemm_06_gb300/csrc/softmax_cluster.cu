@@ -18,6 +18,7 @@
 //    ld.shared::cluster) between cluster barriers.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -384,18 +385,21 @@ int launch_push_rows(SoftmaxParams sp, int device, cudaStream_t stream) {
 }
 
 template <int EPT, bool VEC>
-int launch_cfg(const SoftmaxParams& sp, int threads, cudaStream_t stream) {
+int launch_cfg(const SoftmaxParams& sp, int threads, int device, cudaStream_t stream) {
     auto kern = softmax_rows_kernel<EPT, VEC>;
-    static std::once_flag once;
-    static bool ok = true;
-    std::call_once(once, [&] {
+    // The cluster-size attribute belongs to the current device: set it once
+    // per device (bit d of `tried`; bit d of `failed` if it was refused).
+    static std::atomic<uint64_t> tried{0}, failed{0};
+    const uint64_t bit = 1ull << (device & 63);
+    if (!(tried.load() & bit)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess) {
             cudaGetLastError();
-            ok = false;
+            failed.fetch_or(bit);
         }
-    });
-    if (!ok && sp.cs > 8) return kUnsupported;
+        tried.fetch_or(bit);
+    }
+    if ((failed.load() & bit) && sp.cs > 8) return kUnsupported;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -425,7 +429,8 @@ int launch_warp_rows(const SoftmaxParams& sp, cudaStream_t stream) {
 }
 
 template <bool VEC>
-int launch_any(const SoftmaxParams& sp, int ept, int threads, bool warp_rows, cudaStream_t s) {
+int launch_any(const SoftmaxParams& sp, int ept, int threads, bool warp_rows, int device,
+               cudaStream_t s) {
     if (warp_rows) {
         switch (ept) {
             case 4: return launch_warp_rows<4, VEC>(sp, s);
@@ -434,9 +439,9 @@ int launch_any(const SoftmaxParams& sp, int ept, int threads, bool warp_rows, cu
             default: return launch_warp_rows<32, VEC>(sp, s);
         }
     }
-    if (ept == 16) return launch_cfg<16, VEC>(sp, threads, s);
-    if (ept == 32) return launch_cfg<32, VEC>(sp, threads, s);
-    return launch_cfg<64, VEC>(sp, threads, s);
+    if (ept == 16) return launch_cfg<16, VEC>(sp, threads, device, s);
+    if (ept == 32) return launch_cfg<32, VEC>(sp, threads, device, s);
+    return launch_cfg<64, VEC>(sp, threads, device, s);
 }
 
 }  // namespace
@@ -461,8 +466,8 @@ int launch_softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float
         int ept = 4;
         while (ept * 32 < N) ept *= 2;
         sp.cta_cols = (int)N;
-        return vec ? launch_any<true>(sp, ept, 32, true, stream)
-                   : launch_any<false>(sp, ept, 32, true, stream);
+        return vec ? launch_any<true>(sp, ept, 32, true, dev.device, stream)
+                   : launch_any<false>(sp, ept, 32, true, dev.device, stream);
     }
     int cs = 1;
     while ((int64_t)cs * CL_THREADS * CL_EPT < N) cs *= 2;
@@ -473,8 +478,8 @@ int launch_softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float
                     : (sp.cta_cols <= 32 * MAX_THREADS ? 32 : CL_EPT);
     int threads = (sp.cta_cols + ept - 1) / ept;
     threads = (threads + 31) / 32 * 32;
-    return vec ? launch_any<true>(sp, ept, threads, false, stream)
-               : launch_any<false>(sp, ept, threads, false, stream);
+    return vec ? launch_any<true>(sp, ept, threads, false, dev.device, stream)
+               : launch_any<false>(sp, ept, threads, false, dev.device, stream);
 }
 
 }  // namespace libgemm
