@@ -384,30 +384,44 @@ CPU_ROWS = 400  # rows of each 8192^3 GEMM the oracle computes per sample (~10 s
 REF_ROWS = 256
 
 
-def oracle_sample(f32, bf, rows_per_gemm):
+def oracle_sample(f32, bf, rows_per_gemm, per_gemm=None):
     """The oracle on `rows_per_gemm` seeded rows of each of the step's GEMMs;
-    returns (flops, seconds)."""
+    returns (flops, seconds). per_gemm, if a list, receives (name, seconds)."""
     import datagen
     import oracle
     n = NDIM
     rows = datagen.sample_indices(n, rows_per_gemm, seed=55, always=())
     t0 = time.perf_counter()
-    for _, am, bm in GEMMS:
+    for name, am, bm in GEMMS:
+        t = time.perf_counter()
         oracle.gemm_ref(n, n, n, f32[f"A{am}"].ravel(), n, am, "f32", f32[f"B{bm}"].ravel(), n,
                         bm, "f32", rows=rows)
+        if per_gemm is not None:
+            per_gemm.append((name, time.perf_counter() - t))
+    t = time.perf_counter()
     oracle.gemm_ref(n, n, n, bf["A"].ravel(), n, 0, "bf16", bf["B"].ravel(), n, 0, "bf16",
                     rows=rows)
+    if per_gemm is not None:
+        per_gemm.append(("bf16->bf16 A K-major B K-major", time.perf_counter() - t))
     dt = time.perf_counter() - t0
     return 2.0 * len(rows) * n * n * (len(GEMMS) + 1), dt
 
 
 def cpu_baseline(f32, bf):
+    """The oracle's rate on a bounded sample of every GEMM of the step, and
+    each GEMM's full 8192^3 time extrapolated from it (2 M N K / rate)."""
     import oracle
-    flops, dt = oracle_sample(f32, bf, CPU_ROWS)
+    per = []
+    flops, dt = oracle_sample(f32, bf, CPU_ROWS, per)
+    one = 2.0 * CPU_ROWS * NDIM * NDIM
+    full = 2.0 * NDIM ** 3
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{CPU_ROWS} seeded rows (all 8192 columns) of each of the step's 5 GEMMs "
-                      f"({flops:.3g} flop, {dt:.1f} s), fp64 triple loop"}
+                      f"({flops:.3g} flop, {dt:.1f} s), fp64 triple loop",
+            "per_gemm": [{"gemm": name, "gflops_fp64": round(one / t / 1e9, 2),
+                          "extrapolated_full_s": round(full / (one / t), 1)}
+                         for name, t in per]}
 
 
 def run_reference(args):

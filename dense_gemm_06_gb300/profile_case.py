@@ -43,6 +43,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=sorted(CASES), required=True)
     ap.add_argument("--n", type=int, default=None, help="override M = N = K")
+    ap.add_argument("--shape", type=int, nargs=3, metavar=("M", "N", "K"), default=None,
+                    help="override M, N and K")
     ap.add_argument("--am", type=int, default=None)
     ap.add_argument("--bm", type=int, default=None)
     ap.add_argument("--cta-group", type=int, default=0)
@@ -59,6 +61,8 @@ def main(argv=None):
     M, N, K, dtype, am, bm, dist, seed, lo, hi = CASES[a.case]
     if a.n:
         M = N = K = a.n
+    if a.shape:
+        M, N, K = a.shape
     am = am if a.am is None else a.am
     bm = bm if a.bm is None else a.bm
     it, ot = lg.IN_TYPE[dtype], lg.OUT_TYPE[dtype]

@@ -208,6 +208,7 @@ def test_sgemm_split_tail_forced(config, am, bm, cm):
 
 @pytest.mark.parametrize("am,bm", [(0, 0), (1, 1)])
 def test_sgemm_split_tail_automatic(am, bm):
-    # 20 x 16 = 320 tiles on 2 x 152 CTA slots: a 16-tile last wave, split 4 ways
+    # 20 x 16 = 320 tiles on 152 SMs: two full rounds and 16 tail tiles; with
+    # 69 k-tiles the automatic rule cuts the tail into 2 slices
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL) == 0
-    run_and_check(2557, 2043, 300, lg.GEMM_F32, am, bm, 1, dist="int", seed=46)
+    run_and_check(2557, 2043, 1100, lg.GEMM_F32, am, bm, 1, dist="int", seed=46)
