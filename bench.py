@@ -407,6 +407,36 @@ def oracle_sample(f32, bf, rows_per_gemm, per_gemm=None):
     return 2.0 * len(rows) * n * n * (len(GEMMS) + 1), dt
 
 
+# The smaller workloads of the benchmark definition, which the oracle runs in
+# full for the per-workload baseline: (name, M, N, K, in type, a_major,
+# b_major, distribution, seed, lo, hi).
+SMALL_WORKLOADS = [
+    ("fp16 int 1024x512x256, A K B K", 1024, 512, 256, "f16", 0, 0, "int", 1025, -5, 5),
+    ("fp32 2048^3, A M B N", 2048, 2048, 2048, "f32", 1, 1, "pm1", 1026, 0, 0),
+    ("fp16 int 4095x3071x1037, A K B N", 4095, 3071, 1037, "f16", 0, 1, "int", 1029, -3, 3),
+    ("fp16 int 16384x256x8192, A K B N", 16384, 256, 8192, "f16", 0, 1, "int", 1030, -3, 3),
+]
+
+
+def oracle_small_workloads():
+    """The oracle's fp64 rate on each small workload, computed in full."""
+    import datagen
+    import oracle
+    out = []
+    for name, M, N, K, it, am, bm, dist, seed, lo, hi in SMALL_WORKLOADS:
+        lda, ldb = (K if am == 0 else M), (K if bm == 0 else N)
+        A = datagen.operand(M, K, major=am, ld=lda, dtype=it, dist=dist, seed=seed, stream=0,
+                            lo=lo, hi=hi)
+        B = datagen.operand(N, K, major=bm, ld=ldb, dtype=it, dist=dist, seed=seed, stream=1,
+                            lo=lo, hi=hi)
+        t = time.perf_counter()
+        oracle.gemm_ref(M, N, K, A, lda, am, it, B, ldb, bm, it, with_s=False)
+        dt = time.perf_counter() - t
+        out.append({"workload": name, "seconds": round(dt, 3),
+                    "gflops_fp64": round(2.0 * M * N * K / dt / 1e9, 2), "sample": "full"})
+    return out
+
+
 def cpu_baseline(f32, bf):
     """The oracle's rate on a bounded sample of every GEMM of the step, and
     each GEMM's full 8192^3 time extrapolated from it (2 M N K / rate)."""
@@ -421,7 +451,8 @@ def cpu_baseline(f32, bf):
                       f"({flops:.3g} flop, {dt:.1f} s), fp64 triple loop",
             "per_gemm": [{"gemm": name, "gflops_fp64": round(one / t / 1e9, 2),
                           "extrapolated_full_s": round(full / (one / t), 1)}
-                         for name, t in per]}
+                         for name, t in per],
+            "per_small_workload": oracle_small_workloads()}
 
 
 def run_reference(args):
