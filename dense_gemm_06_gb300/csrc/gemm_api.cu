@@ -575,12 +575,15 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
                                      c_major, dtype);
         const RunConfig cfg = resolve(make_key(M, N, K, dA, lda_d, a_major, dB, ldb_d, b_major,
                                                dC, ldc_d, c_major, dtype));
-        const int64_t rows = host_panel_rows(pd, *dev, cfg);
-        const int panels = (int)((pd.M + rows - 1) / rows);
+        // host_panel_rows gives at most about 8 panels; more than kMaxPanels
+        // would only come from a model error, and then the call runs whole.
+        constexpr int kMaxPanels = 64;
+        int64_t rows = host_panel_rows(pd, *dev, cfg);
+        if ((pd.M + rows - 1) / rows > kMaxPanels) rows = pd.M;
+        const int np = (int)((pd.M + rows - 1) / rows);
 
         // Events: allocation done (s), B (and A unless it goes by panels)
         // in, each A panel in, each C panel computed, both copy streams done.
-        constexpr int kMaxPanels = 64;
         cudaEvent_t ev[2 * kMaxPanels + 4] = {};
         int nev = 0;
         auto event = [&]() -> cudaEvent_t {
@@ -599,12 +602,12 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         };
         // A panel of A's rows is one copy of contiguous rows when A (in the
         // normalised problem) is K-major; otherwise A goes in whole with B.
-        const bool a_panels = panels > 1 && pd.a_kmajor && panels <= kMaxPanels;
-        const int np = a_panels || panels <= kMaxPanels ? panels : 1;
-        const int64_t prow = np == 1 ? pd.M : rows;
+        const bool a_panels = np > 1 && pd.a_kmajor;
+        const int64_t prow = rows;
         cudaEvent_t e_alloc = event(), e_b = event();
         if (!e_alloc || !e_b) rc = kCuda;
-        if (ok(cudaEventRecord(e_alloc, s)) && ok(cudaStreamWaitEvent(h2d, e_alloc, 0)) && K > 0) {
+        if (rc == kOk && ok(cudaEventRecord(e_alloc, s)) &&
+            ok(cudaStreamWaitEvent(h2d, e_alloc, 0)) && K > 0) {
             const char* hB = static_cast<const char*>(ph.B);
             char* dBp = static_cast<char*>(const_cast<void*>(pd.B));
             const int64_t bi = pd.b_kmajor ? K : pd.N, bo = pd.b_kmajor ? pd.N : K;
