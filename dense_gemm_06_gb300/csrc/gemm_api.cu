@@ -602,8 +602,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         };
         // A panel of A's rows is one copy of contiguous rows when A (in the
         // normalised problem) is K-major; otherwise A goes in whole with B.
-        const bool a_panels = np > 1 && pd.a_kmajor;
+        const bool a_panels = np > 1;  // A goes in panel by panel (either major)
         const int64_t prow = rows;
+        Problem pb = pd;             // B replaced by its MN-major copy, if made
+        void* bt = nullptr;
         cudaEvent_t e_alloc = event(), e_b = event();
         if (!e_alloc || !e_b) rc = kCuda;
         if (rc == kOk && ok(cudaEventRecord(e_alloc, s)) &&
@@ -612,7 +614,7 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
             char* dBp = static_cast<char*>(const_cast<void*>(pd.B));
             const int64_t bi = pd.b_kmajor ? K : pd.N, bo = pd.b_kmajor ? pd.N : K;
             ok(copy(dBp, pd.ldb * ie, hB, ph.ldb * ie, bi * ie, bo, cudaMemcpyHostToDevice, h2d));
-            if (!a_panels) {
+            if (!a_panels) {  // one panel: all of A with B
                 const int64_t ai = pd.a_kmajor ? K : pd.M, ao = pd.a_kmajor ? pd.M : K;
                 ok(copy(const_cast<void*>(pd.A), pd.lda * ie, ph.A, ph.lda * ie, ai * ie, ao,
                         cudaMemcpyHostToDevice, h2d));
@@ -620,18 +622,43 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         }
         if (rc == kOk) ok(cudaEventRecord(e_b, h2d));
         if (rc == kOk) ok(cudaStreamWaitEvent(s, e_b, 0));
+        // A K-major fp32 B that every panel would transpose for the FFMA
+        // kernel is transposed once here instead.
+        if (rc == kOk && np > 1 && K > 0 && dtype == GEMM_F32 && pd.b_kmajor) {
+            Problem q0 = pd;
+            q0.M = prow;
+            if (want_transpose(q0.M, q0, cfg.simt_transpose)) {
+                const int64_t ld2 = round_up(pd.N, 4);
+                if (cudaMallocFromPoolAsync(&bt, (size_t)(K * ld2 * 4), pool, s) != cudaSuccess) {
+                    cudaGetLastError();
+                    bt = nullptr;
+                    rc = kCuda;
+                } else {
+                    rc = launch_transpose_f32(static_cast<const float*>(pd.B), pd.ldb,
+                                              static_cast<float*>(bt), ld2, pd.N, K, *dev, s);
+                    pb.B = bt;
+                    pb.ldb = ld2;
+                    pb.b_kmajor = false;
+                }
+            }
+        }
         for (int i = 0; i < np && rc == kOk; ++i) {
             const int64_t m0 = i * prow, m1 = std::min<int64_t>(pd.M, m0 + prow);
-            Problem q = pd;
+            Problem q = pb;
             q.M = m1 - m0;
             q.C = static_cast<char*>(pd.C) + m0 * pd.ldc * oe;
             if (K > 0) q.A = static_cast<const char*>(pd.A) + (pd.a_kmajor ? m0 * pd.lda : m0) * ie;
             if (a_panels && K > 0) {
                 cudaEvent_t e_a = event();
                 if (!e_a) { rc = kCuda; break; }
-                ok(copy(const_cast<void*>(q.A), pd.lda * ie,
-                        static_cast<const char*>(ph.A) + m0 * ph.lda * ie, ph.lda * ie, K * ie,
-                        q.M, cudaMemcpyHostToDevice, h2d));
+                if (pd.a_kmajor)  // rows m0 .. m1 of A
+                    ok(copy(const_cast<void*>(q.A), pd.lda * ie,
+                            static_cast<const char*>(ph.A) + m0 * ph.lda * ie, ph.lda * ie,
+                            K * ie, q.M, cudaMemcpyHostToDevice, h2d));
+                else              // columns m0 .. m1 of every k-row of A
+                    ok(copy(const_cast<void*>(q.A), pd.lda * ie,
+                            static_cast<const char*>(ph.A) + m0 * ie, ph.lda * ie, q.M * ie, K,
+                            cudaMemcpyHostToDevice, h2d));
                 if (rc == kOk) ok(cudaEventRecord(e_a, h2d));
                 if (rc == kOk) ok(cudaStreamWaitEvent(s, e_a, 0));
             }
@@ -652,6 +679,7 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         if (e_out && cudaEventRecord(e_out, d2h) == cudaSuccess) cudaStreamWaitEvent(s, e_out, 0);
         else rc = rc == kOk ? kCuda : rc;
         cudaGetLastError();
+        if (bt) cudaFreeAsync(bt, s);
         if (dA) cudaFreeAsync(dA, s);
         if (dB) cudaFreeAsync(dB, s);
         cudaFreeAsync(dC, s);
