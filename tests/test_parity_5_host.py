@@ -1,9 +1,9 @@
 """GPU parity of gemm_host (host buffers in and out) against the oracle.
 
-Small problems run as one panel; large ones are cut into row panels whose
-A rows go in, compute and C rows come back on separate copy streams, so the
-cases below cover one and several panels, every C major, K-major and
-MN-major A (A by panels or whole), padded leading dimensions, pinned and
+Small problems run as one panel; large ones are cut into row panels of C
+whose A rows (or columns) go in, compute and C rows come back on separate
+copy streams, so the cases below cover one and several panels, every C
+major, K- and MN-major A and B, padded leading dimensions, pinned and
 pageable host memory, and K = 0. Integer-valued inputs: compared bit-exactly
 (16-bit C: against round-to-nearest-even of C_ref)."""
 
@@ -84,10 +84,12 @@ def test_host_one_panel(dtype, am, bm, cm):
 
 @pytest.mark.parametrize("dtype,M,N,K", [(lg.GEMM_F32, 4096, 2048, 2048),
                                          (lg.GEMM_BF16_F32, 8192, 2048, 1024),
-                                         (lg.GEMM_F16_F16, 8192, 2048, 1024)])
+                                         (lg.GEMM_F16_F16, 8192, 2048, 1024),
+                                         (lg.GEMM_F32, 2560, 8192, 1024),
+                                         (lg.GEMM_BF16_BF16, 8192, 4096, 1024)])
 @pytest.mark.parametrize("am,cm", [(0, 1), (1, 1), (0, 0), (1, 0)])
 def test_host_several_panels(dtype, M, N, K, am, cm):
-    # M * N * K >= 1e10: the rows of C go in whole waves of tiles, 2+ panels
+    # M * N * K >= 1e10: row panels of C in whole waves of tiles
     C, A, lda, B, ldb = host_gemm(M, N, K, dtype, am, 1 - am, cm, seed=51, pinned=(am == 0))
     it, ot = lg.IN_TYPE[dtype], lg.OUT_TYPE[dtype]
     rows = datagen.sample_indices(M, 128, seed=52, stream=101)
