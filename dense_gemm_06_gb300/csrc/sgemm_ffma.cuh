@@ -47,6 +47,10 @@ int launch_sgemm_cfg7(const SgemmParams& sp, int av, int bv, int device, int sm_
 int launch_sgemm_cfg8(const SgemmParams& sp, int av, int bv, int device, int sm_count,
                       int split_mode, Scratch* scratch, cudaStream_t s);
 
+// Chooses the K-split of the tail tiles (defined in sgemm_ffma.cu, with the
+// model it uses); fills sp.dp_tiles, sp.splits and sp.kt_slice.
+void plan_split(SgemmParams& sp, int slots, int sm_count, int nkt, int split_mode);
+
 namespace {
 
 
@@ -416,52 +420,6 @@ bool configure_once(Kern kern, std::atomic<uint64_t>& done, int device, int smem
         return false;
     done.fetch_or(bit);
     return true;
-}
-
-// Chooses the K-split of the tail tiles. Model: an SM finishes the same
-// tile work per unit of time whether it holds one CTA or two, so a launch
-// takes (most tile-units on one SM) x (work of a unit). With P SMs and T
-// tiles, q = T / P full rounds and r = T mod P tail tiles: whole, the tail
-// adds one round; cut into s K-slices (one CTA each), it adds
-// ceil(r s / P) / s. Automatic: when there are at least two full rounds,
-// the s in 2..8 (slices of at least 32 k-tiles: shorter ones spend too much
-// of their time filling the pipeline and writing partial sums, measured at
-// 2048^3) with the shortest time, if that saves at least 10% against no
-// split. split_mode 2 (tests)
-// always cuts the last wave of `slots` CTAs (all tiles if T < slots) into
-// at least 2 slices.
-void plan_split(SgemmParams& sp, int slots, int sm_count, int nkt, int split_mode) {
-    const int64_t T = (int64_t)sp.tiles_m * sp.tiles_n;
-    sp.dp_tiles = (int)T;
-    sp.splits = 1;
-    sp.kt_slice = nkt;
-    if (split_mode == 1 || slots <= 0 || sm_count <= 0 || T <= 0) return;
-    if (split_mode == 2) {
-        int64_t r = T % slots;
-        if (r == 0) r = T < slots ? T : slots;
-        int s = (int)(slots / r);
-        s = s < 2 ? 2 : (s > 4 ? 4 : s);
-        sp.dp_tiles = (int)(T - r);
-        sp.splits = s;
-        sp.kt_slice = (nkt + s - 1) / s;
-        return;
-    }
-    const int64_t P = sm_count, q = T / P, r = T % P;
-    if (r == 0 || q < 2) return;
-    const double whole = (double)(q + 1);
-    double best = whole;
-    int best_s = 1;
-    for (int s = 2; s <= 8 && nkt >= 32 * s; ++s) {
-        const double t = (double)q + (double)((r * s + P - 1) / P) / s;
-        if (t < best - 1e-9) {
-            best = t;
-            best_s = s;
-        }
-    }
-    if (best_s == 1 || best > 0.9 * whole) return;
-    sp.dp_tiles = (int)(T - r);
-    sp.splits = best_s;
-    sp.kt_slice = (nkt + best_s - 1) / best_s;
 }
 
 template <class Cfg, bool A_K, int A_VEC, bool B_K, int B_VEC>

@@ -206,9 +206,11 @@ def test_sgemm_split_tail_forced(config, am, bm, cm):
             lg.gemm_set_option(o, v)
 
 
+@pytest.mark.parametrize("M,N,K", [(2557, 2043, 1100), (1000, 1001, 1100)])
 @pytest.mark.parametrize("am,bm", [(0, 0), (1, 1)])
-def test_sgemm_split_tail_automatic(am, bm):
-    # 20 x 16 = 320 tiles on 152 SMs: two full rounds and 16 tail tiles; with
-    # 69 k-tiles the automatic rule cuts the tail into 2 slices
+def test_sgemm_split_tail_automatic(am, bm, M, N, K):
+    # 2557 x 2043: 320 tiles on 152 SMs, two full rounds and 16 tail tiles;
+    # 1000 x 1001: 64 tiles, no full round. With 69 k-tiles the automatic
+    # rule cuts the tail into 2 slices in both.
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL) == 0
-    run_and_check(2557, 2043, 1100, lg.GEMM_F32, am, bm, 1, dist="int", seed=46)
+    run_and_check(M, N, K, lg.GEMM_F32, am, bm, 1, dist="int", seed=46)
