@@ -201,12 +201,8 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_
 
 __global__ void zero_rows_kernel(uint8_t* C, int64_t rows, int64_t row_bytes,
                                  int64_t pitch_bytes) {
-    const int64_t total = rows * row_bytes;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / row_bytes, c = i - r * row_bytes;
-        C[r * pitch_bytes + c] = 0;
-    }
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)  // a block per row
+        for (int64_t c = threadIdx.x; c < row_bytes; c += blockDim.x) C[r * pitch_bytes + c] = 0;
 }
 
 // Copy `outer` rows of `inner` 16-bit elements (src row pitch `lds`) into dst
@@ -214,12 +210,14 @@ __global__ void zero_rows_kernel(uint8_t* C, int64_t rows, int64_t row_bytes,
 __global__ void repack16_kernel(const uint16_t* __restrict__ src, int64_t lds,
                                 uint16_t* __restrict__ dst, int64_t ldd, int64_t outer,
                                 int64_t inner) {
-    const int64_t total = outer * inner;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / inner, c = i - r * inner;
-        dst[r * ldd + c] = src[r * lds + c];
-    }
+    for (int64_t r = blockIdx.x; r < outer; r += gridDim.x)  // a block per row
+        for (int64_t c = threadIdx.x; c < inner; c += blockDim.x) dst[r * ldd + c] = src[r * lds + c];
+}
+
+// Blocks for a row-per-block kernel over `rows` rows: at most 8 per SM.
+int grid_rows(int64_t rows, const DeviceInfo& dev) {
+    const int64_t cap = (int64_t)dev.sm_count * 8;
+    return (int)(rows < 1 ? 1 : (rows > cap ? cap : rows));
 }
 
 int grid_for(int64_t work, const DeviceInfo& dev) {
@@ -232,8 +230,8 @@ int grid_for(int64_t work, const DeviceInfo& dev) {
 int zero_fill(void* C, int64_t rows, int64_t cols, int64_t ld, int esize, const DeviceInfo& dev,
               cudaStream_t s) {
     const int64_t rb = cols * esize;
-    zero_rows_kernel<<<grid_for(rows * rb, dev), 256, 0, s>>>(static_cast<uint8_t*>(C), rows,
-                                                               rb, ld * esize);
+    zero_rows_kernel<<<grid_rows(rows, dev), 256, 0, s>>>(static_cast<uint8_t*>(C), rows, rb,
+                                                           ld * esize);
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     note_launch();
     return kOk;
@@ -328,7 +326,7 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCo
             rc = kCuda;
             break;
         }
-        repack16_kernel<<<grid_for(outer * inner, dev), 256, 0, s>>>(
+        repack16_kernel<<<grid_rows(outer, dev), 256, 0, s>>>(
             static_cast<const uint16_t*>(*ops[i]), *lds[i], static_cast<uint16_t*>(scratch[i]),
             ld2, outer, inner);
         if (cudaGetLastError() != cudaSuccess) { rc = kCuda; break; }

@@ -90,23 +90,15 @@ int fixed_device(FixedDevice** out) {
 __global__ void repack16_fixed_kernel(const uint16_t* __restrict__ src, int64_t lds,
                                       int64_t off, int64_t ldd, int64_t outer, int64_t inner) {
     uint16_t* dst = reinterpret_cast<uint16_t*>(g_fixed_scratch + off);
-    const int64_t total = outer * inner;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / inner, c = i - r * inner;
-        dst[r * ldd + c] = src[r * lds + c];
-    }
+    for (int64_t r = blockIdx.x; r < outer; r += gridDim.x)  // a block per row
+        for (int64_t c = threadIdx.x; c < inner; c += blockDim.x) dst[r * ldd + c] = src[r * lds + c];
 }
 
 // C = 0 for K == 0: `rows` rows of `row_bytes` bytes, `pitch` bytes apart.
 __global__ void zero_fixed_kernel(unsigned char* C, int64_t rows, int64_t row_bytes,
                                   int64_t pitch) {
-    const int64_t total = rows * row_bytes;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / row_bytes;
-        C[r * pitch + (i - r * row_bytes)] = 0;
-    }
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)  // a block per row
+        for (int64_t c = threadIdx.x; c < row_bytes; c += blockDim.x) C[r * pitch + c] = 0;
 }
 
 bool rows_tma_ready(const void* p, int64_t ld) {
@@ -133,7 +125,7 @@ extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int6
             rc = fixed_device(&fd);
             if (rc != kOk) return rc;
             const int64_t esize = dtype <= GEMM_BF16_F32 ? 4 : 2;
-            int64_t blocks = (p.M * p.N * esize + 255) / 256;
+            int64_t blocks = p.M;  // a block per row of C
             const int64_t cap = (int64_t)fd->info.sm_count * 8;
             if (blocks > cap) blocks = cap;
             zero_fixed_kernel<<<(int)(blocks < 1 ? 1 : blocks), 256, 0,
@@ -169,7 +161,7 @@ extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int6
         cudaStream_t s = static_cast<cudaStream_t>(stream);
         for (int i = 0; i < 2; ++i) {
             if (off[i] < 0) continue;
-            int64_t blocks = (outer[i] * inner[i] + 255) / 256;
+            int64_t blocks = outer[i];  // a block per row
             const int64_t cap = (int64_t)fd->info.sm_count * 8;
             if (blocks > cap) blocks = cap;
             repack16_fixed_kernel<<<(int)(blocks < 1 ? 1 : blocks), 256, 0, s>>>(
