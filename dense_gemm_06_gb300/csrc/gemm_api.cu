@@ -220,12 +220,6 @@ int grid_rows(int64_t rows, const DeviceInfo& dev) {
     return (int)(rows < 1 ? 1 : (rows > cap ? cap : rows));
 }
 
-int grid_for(int64_t work, const DeviceInfo& dev) {
-    int64_t blocks = (work + 255) / 256;
-    const int64_t cap = (int64_t)dev.sm_count * 8;
-    if (blocks > cap) blocks = cap;
-    return (int)(blocks < 1 ? 1 : blocks);
-}
 
 int zero_fill(void* C, int64_t rows, int64_t cols, int64_t ld, int esize, const DeviceInfo& dev,
               cudaStream_t s) {
@@ -388,20 +382,18 @@ namespace {
 // C = act(beta * C + bias) for K == 0 (the product term is zero).
 template <typename OutT>
 __global__ void epilogue_only_kernel(OutT* C, int64_t ldc, int rows, int cols, EpiParams e) {
-    const int64_t total = (int64_t)rows * cols;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int r = (int)(i / cols), c = (int)(i - (int64_t)r * cols);
-        OutT* d = C + (int64_t)r * ldc + c;
-        const float old = e.beta != 0.f ? to_f32(*d) : 0.f;
-        *d = from_f32<OutT>(epilogue_value<OutT>(e, 0.f, old, r, c));
-    }
+    for (int r = blockIdx.x; r < rows; r += gridDim.x)  // a block per row
+        for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+            OutT* d = C + (int64_t)r * ldc + c;
+            const float old = e.beta != 0.f ? to_f32(*d) : 0.f;
+            *d = from_f32<OutT>(epilogue_value<OutT>(e, 0.f, old, r, c));
+        }
 }
 
 }  // namespace
 
 int launch_epilogue_only(const Problem& p, const DeviceInfo& dev, cudaStream_t s) {
-    const int grid = grid_for(p.M * p.N, dev);
+    const int grid = grid_rows(p.M, dev);
     if (out_bytes(p.dtype) == 4)
         epilogue_only_kernel<float><<<grid, 256, 0, s>>>(static_cast<float*>(p.C), p.ldc,
                                                           (int)p.M, (int)p.N, p.epi);
