@@ -42,9 +42,21 @@ FLOPS_PER_GEMM = 2.0 * NDIM ** 3
 WORKLOAD = ("8192^3 fp32 SGEMM x 4 A/B majors (C N-major, FFMA kernel) + 8192^3 bf16->bf16 "
             "GEMM (A,B K-major, tcgen05 2-CTA kernel); one step = these 5 GEMMs")
 
-# Peaks. FFMA: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz (max SM clock).
+# Peaks. FFMA: SMs x 128 fp32 lanes x 2 flop x maximum SM clock, from the SM
+# count the device reports and the maximum clock nvidia-smi reports during the
+# run; GB300's 152 SMs and 2.07 GHz when either is unavailable.
 SMS, FP32_LANES, SM_MAX_GHZ = 152, 128, 2.07
 FFMA_PEAK_TFLOPS = SMS * FP32_LANES * 2 * SM_MAX_GHZ / 1e3
+SGEMM_KERNEL = "sgemm_ffma_tma_kernel"  # the FFMA kernel the step's fp32 GEMMs run
+
+
+def ffma_peak(sm_count, sm_max_mhz):
+    """(TFLOP/s, how it was obtained) of the FP32 FFMA pipe."""
+    sms = int(sm_count) if sm_count else SMS
+    ghz = float(sm_max_mhz) / 1e3 if sm_max_mhz else SM_MAX_GHZ
+    how = (f"derived: {sms} SMs ({'queried' if sm_count else 'assumed'}) x {FP32_LANES} FP32 "
+           f"lanes x 2 x {ghz:.3g} GHz ({'nvidia-smi max SM clock' if sm_max_mhz else 'assumed'})")
+    return sms * FP32_LANES * 2 * ghz / 1e3, how
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -233,14 +245,16 @@ def run_native(args):
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
+    ffma_tf, ffma_how = ffma_peak(torch.cuda.get_device_properties(dev).multi_processor_count,
+                                  (clocks or {}).get("sm_max_mhz"))
     flops_step = FLOPS_PER_GEMM * n_gemms
     value = throughput_tflops(flops_step, args.steps, world, ms_total)
     parts = []
     for i, (name, am, bm) in enumerate(GEMMS):
         tf = FLOPS_PER_GEMM / (per_ms[i] * 1e-3) / 1e12
-        parts.append({"gemm": name, "kernel": "sgemm_ffma_kernel", "ms": round(per_ms[i], 4),
-                      "tflops": round(tf, 2), "peak_tflops": round(FFMA_PEAK_TFLOPS, 2),
-                      "peak_kind": "alu (FFMA, derived)", "frac": round(tf / FFMA_PEAK_TFLOPS, 4)})
+        parts.append({"gemm": name, "kernel": SGEMM_KERNEL, "ms": round(per_ms[i], 4),
+                      "tflops": round(tf, 2), "peak_tflops": round(ffma_tf, 2),
+                      "peak_kind": "alu (FFMA, derived)", "frac": round(tf / ffma_tf, 4)})
     tf16 = FLOPS_PER_GEMM / (per_ms[-1] * 1e-3) / 1e12
     parts.append({"gemm": "bf16->bf16 A K-major B K-major", "kernel": "gemm_tc_kernel",
                   "ms": round(per_ms[-1], 4), "tflops": round(tf16, 2),
@@ -249,11 +263,11 @@ def run_native(args):
                   "frac_of_sustained": round(tf16 / peaks["bf16_tflops_sustained"], 4)})
     sgemm_ms = float(np.mean(per_ms[:4]))
     achieved = FLOPS_PER_GEMM / (sgemm_ms * 1e-3) / 1e12
-    roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FFMA_PEAK_TFLOPS, 2),
-                "unit": "TFLOP/s", "frac": round(achieved / FFMA_PEAK_TFLOPS, 4),
-                "traffic": profiled_traffic("sgemm_ffma_kernel"),
-                "kernel": "sgemm_ffma_kernel",
-                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"}
+    roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(ffma_tf, 2),
+                "unit": "TFLOP/s", "frac": round(achieved / ffma_tf, 4),
+                "traffic": profiled_traffic(SGEMM_KERNEL),
+                "kernel": SGEMM_KERNEL,
+                "peak_source": ffma_how}
     roofline_tc = {"bound": "tensor", "achieved": round(tf16, 2), "peak": peaks["bf16_tflops"],
                    "unit": "TFLOP/s", "frac": round(tf16 / peaks["bf16_tflops"], 4),
                    "traffic": profiled_traffic("gemm_tc_kernel"), "kernel": "gemm_tc_kernel",
@@ -367,12 +381,15 @@ def profiled_traffic(kernel: str):
             entry = json.load(f)[kernel]
     except Exception:
         return None
-    src = os.path.join(ROOT, "dense_gemm_06_gb300", "csrc", entry["source"])
+    names = entry["source"] if isinstance(entry["source"], list) else [entry["source"]]
+    h = hashlib.sha256()
     try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        for name in names:  # the kernel's sources, hashed in the listed order
+            with open(os.path.join(ROOT, "dense_gemm_06_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
     except OSError:
         return None
+    digest = h.hexdigest()[:16]
     return entry["bytes_per_launch"] if digest == entry["source_sha256_16"] else None
 
 

@@ -38,6 +38,7 @@ std::atomic<int> g_softmax_fault_inject{0};
 std::atomic<int> g_simt_config{0};
 std::atomic<int> g_simt_transpose{0};
 std::atomic<int> g_simt_split{0};
+std::atomic<int> g_simt_fault_inject{0};
 std::atomic<int> g_tc_scheduler{0};
 std::atomic<int> g_tc_store{0};
 std::atomic<int> g_tc_multicast{0};
@@ -46,7 +47,7 @@ std::atomic<int> g_tc_multicast{0};
 // (no "automatic" values): an option set to a non-zero value wins, then a
 // gemm_tune() entry for the problem, then the built-in choice.
 struct RunConfig {
-    int simt_config;     // 1..8
+    int simt_config;     // 1..9
     int simt_transpose;  // 0 automatic size rule, 1 never, 2 always
     int cta_group;       // 1 or 2
     int multicast;       // 1 off, 2 on
@@ -290,7 +291,9 @@ int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCon
         *kmaj[i] = false;
     }
     Scratch tail{pool, s};
-    if (rc == kOk) rc = launch_sgemm_f32(p, dev, cfg.simt_config, cfg.simt_split, &tail, s);
+    if (rc == kOk)
+        rc = launch_sgemm_f32(p, dev, cfg.simt_config, cfg.simt_split, &tail,
+                              g_wait_limit_ns.load(), g_simt_fault_inject.load(), s);
     if (tail.ptr) cudaFreeAsync(tail.ptr, s);
     for (int i = 0; i < 2; ++i)
         if (scratch[i]) cudaFreeAsync(scratch[i], s);
@@ -364,7 +367,7 @@ RunConfig resolve(const TuneKey& key) {
             tuned = true;
         }
     }
-    if (c.simt_config == 0) c.simt_config = tuned && t.simt_config ? t.simt_config : 7;
+    if (c.simt_config == 0) c.simt_config = tuned && t.simt_config ? t.simt_config : 9;
     if (c.simt_transpose == 0 && tuned) c.simt_transpose = t.simt_transpose;
     if (c.cta_group == 0) c.cta_group = tuned && t.tc_cta_group ? t.tc_cta_group : 2;
     if (c.multicast == 0) c.multicast = tuned && t.tc_multicast ? t.tc_multicast : 1;
@@ -703,7 +706,7 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         int n = 0;
         if (dtype == GEMM_F32) {
             const bool any_kmajor = p.a_kmajor || p.b_kmajor;
-            for (int c = 1; c <= 8; ++c)
+            for (int c = 1; c <= 9; ++c)
                 for (int t = 1; t <= (any_kmajor ? 2 : 1); ++t) cands[n++] = {c, t, 2, 1, 0};
         } else {
             const bool c_aligned = aligned16_ld(C, ldc, out_bytes(dtype));
@@ -854,7 +857,7 @@ int gemm_set_option(int option, int64_t value) {
             g_fault_inject.store((int)value);
             return GEMM_OK;
         case GEMM_OPT_SIMT_CONFIG:
-            if (value < 0 || value > 8) return GEMM_ERR_INVALID_ARG;
+            if (value < 0 || value > 9) return GEMM_ERR_INVALID_ARG;
             g_simt_config.store((int)value);
             return GEMM_OK;
         case GEMM_OPT_SIMT_TRANSPOSE:
@@ -881,6 +884,10 @@ int gemm_set_option(int option, int64_t value) {
             if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             g_tc_scheduler.store((int)value);
             return GEMM_OK;
+        case GEMM_OPT_SIMT_FAULT_INJECT:
+            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            g_simt_fault_inject.store((int)value);
+            return GEMM_OK;
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -897,6 +904,7 @@ int64_t gemm_get_option(int option) {
         case GEMM_OPT_SOFTMAX_FAULT_INJECT: return g_softmax_fault_inject.load();
         case GEMM_OPT_SIMT_SPLIT_TAIL: return g_simt_split.load();
         case GEMM_OPT_TC_SCHEDULER: return g_tc_scheduler.load();
+        case GEMM_OPT_SIMT_FAULT_INJECT: return g_simt_fault_inject.load();
         default: return -1;
     }
 }

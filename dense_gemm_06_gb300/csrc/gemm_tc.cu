@@ -87,6 +87,21 @@ bool encode_2d(CUtensorMap* map, bool bf16, const void* ptr, uint64_t inner, uin
 
 }  // namespace
 
+bool encode_tma_f32_2d(void* map, const float* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                       uint32_t box_inner, uint32_t box_outer) {
+    if (!get_encoder()) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld * 4};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                                const_cast<float*>(ptr), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
                    uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled, int multicast,
                    int clc, cudaStream_t stream) {

@@ -60,8 +60,18 @@ struct Scratch {
 };
 // split_mode: 0 automatic (K-split the last wave's tiles when it is at most
 // half full), 1 never, 2 always split the last wave (tests).
+// wait_limit_ns / fault_inject: the bounded mbarrier waits of configuration 9
+// (TMA-fed) and its test hook (1 = the first CTA never loads its second
+// k-tile, so its waits run out and report a timeout in the error word).
 int launch_sgemm_f32(const Problem& p, const DeviceInfo& dev, int config, int split_mode,
-                     Scratch* scratch, cudaStream_t stream);
+                     Scratch* scratch, uint64_t wait_limit_ns, int fault_inject,
+                     cudaStream_t stream);
+// A 2-D TMA tensor map (a 64-byte-aligned CUtensorMap at `map`) over an fp32
+// matrix of `outer` rows of `inner` contiguous elements, `ld` elements
+// apart; box {box_inner, box_outer}, no swizzle, zero fill outside the
+// matrix. False when the driver's encoder is missing or rejects the map.
+bool encode_tma_f32_2d(void* map, const float* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                       uint32_t box_inner, uint32_t box_outer);
 // dst[c * ldd + r] = src[r * lds + c] (fp32), rows x cols.
 int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
                          int64_t cols, const DeviceInfo& dev, cudaStream_t stream);

@@ -127,8 +127,15 @@ int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd,
     return kOk;
 }
 
+// Configuration 9: configuration 7's tile with TMA-fed shared memory when
+// both operands are MN-major and 16-byte aligned (sgemm_cfg9.cu).
+int launch_sgemm_cfg9(const SgemmParams& sp, int av, int bv, const DeviceInfo& dev,
+                      int split_mode, Scratch* scratch, uint64_t wait_limit_ns, int fault_inject,
+                      cudaStream_t s);
+
 int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, int split_mode,
-                     Scratch* scratch, cudaStream_t stream) {
+                     Scratch* scratch, uint64_t wait_limit_ns, int fault_inject,
+                     cudaStream_t stream) {
     SgemmParams sp;
     sp.A = static_cast<const float*>(pr.A);
     sp.B = static_cast<const float*>(pr.B);
@@ -161,6 +168,9 @@ int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, int s
         case 6: return launch_sgemm_cfg6(sp, av, bv, d, n, split_mode, scratch, stream);
         case 7: return launch_sgemm_cfg7(sp, av, bv, d, n, split_mode, scratch, stream);
         case 8: return launch_sgemm_cfg8(sp, av, bv, d, n, split_mode, scratch, stream);
+        case 9:
+            return launch_sgemm_cfg9(sp, av, bv, dev, split_mode, scratch, wait_limit_ns,
+                                     fault_inject, stream);
         default: return launch_sgemm_cfg1(sp, av, bv, d, n, split_mode, scratch, stream);
     }
 }

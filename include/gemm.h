@@ -197,7 +197,7 @@ int gemm_noalloc(int64_t M, int64_t N, int64_t K,
 /* A kernel configuration chosen by gemm_tune (the option values it stands
    for; see enum gemm_option). */
 typedef struct gemm_tuning {
-    int simt_config;    /* fp32: FFMA tile configuration 1..6 */
+    int simt_config;    /* fp32: FFMA tile configuration 1..9 */
     int simt_transpose; /* fp32: 1 = run K-major operands as they are,
                            2 = transpose them to MN-major first */
     int tc_cta_group;   /* 16-bit: 1 or 2 CTAs per tile */
@@ -275,10 +275,11 @@ uint64_t gemm_launch_count(void);
 
 /* Options (process-wide; read at each call). */
 enum gemm_option {
-    /* Time limit of every pipeline barrier wait in the tensor-core kernel, in
-       nanoseconds (default 1000000000; 0 restores the default). A wait that
-       runs past it records GEMM_ERR_TIMEOUT in the device error word and the
-       kernel winds down without further writes to C. */
+    /* Time limit of every pipeline barrier wait in the tensor-core kernel,
+       the TMA-fed FFMA kernel (GEMM_OPT_SIMT_CONFIG 9) and the clustered
+       softmax, in nanoseconds (default 1000000000; 0 restores the default).
+       A wait that runs past it records GEMM_ERR_TIMEOUT in the device error
+       word and the kernel winds down without further writes to C. */
     GEMM_OPT_WAIT_LIMIT_NS = 1,
     /* Tensor-core kernel variant: 0 = automatic (the 2-CTA pair kernel),
        1 = one CTA per tile (cta_group::1, 128 x 256 tiles),
@@ -291,13 +292,17 @@ enum gemm_option {
     GEMM_OPT_TC_FAULT_INJECT = 3,
     /* Tile configuration of the fp32 FFMA kernel (all 128 x 128 CTA tiles),
        as (k-depth, ring stages, FMA form, CTAs per SM the registers are
-       sized for, outputs per thread): 0 = automatic (7, the fastest
+       sized for, outputs per thread): 0 = automatic (9, the fastest
        measured at 8192^3),
        1 = (16, 4, packed, 2, 8 x 8), 2 = (16, 4, scalar, 2, 8 x 8),
        3 = (32, 3, packed, 2, 8 x 8), 4 = (8, 3, packed, 2, 8 x 8) -- the CuTe
        Ampere example's 128 x 128 x 8 with 3 stages --,
        5 = (16, 4, packed, 1, 8 x 8), 6 = (32, 4, packed, 1, 8 x 8),
-       7 = (16, 4, packed, 2, 8 x 16), 8 = (32, 3, packed, 2, 8 x 16).
+       7 = (16, 4, packed, 2, 8 x 16), 8 = (32, 3, packed, 2, 8 x 16),
+       9 = (16, 5, packed, 2, 8 x 16) with shared memory filled by TMA
+       tensor copies and per-stage mbarriers instead of cp.async and a CTA
+       barrier, when A and B (after any transpose) are MN-major with 16-byte
+       aligned bases and row pitches; 7 otherwise.
        8 x 8 runs 256 threads per CTA, 8 x 16 runs 128. "Packed" is the
        two-lane fma.rn.f32x2. Every configuration rounds each multiply-add
        once (IEEE fma) and sums k in the same order. */
@@ -340,7 +345,12 @@ enum gemm_option {
        clusters that have not started with clusterlaunchcontrol.try_cancel,
        a scheduler warp multicasting each response to both CTAs of the pair).
        The operand-multicast variant always uses the static schedule. */
-    GEMM_OPT_TC_SCHEDULER = 10
+    GEMM_OPT_TC_SCHEDULER = 10,
+    /* Test hook for the TMA-fed FFMA kernel's timeout path: 1 makes its
+       first CTA skip the copy of its second k-tile, so that CTA's waits run
+       out after GEMM_OPT_WAIT_LIMIT_NS and gemm_check_device_error reports
+       GEMM_ERR_TIMEOUT; C is then undefined. 0 (default) = off. */
+    GEMM_OPT_SIMT_FAULT_INJECT = 11
 };
 
 /* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */

@@ -90,6 +90,11 @@ def test_peaks_file_or_fallback():
     assert src in ("measured", "fallback")
     assert peaks["bf16_tflops"] > 1000 and peaks["hbm_gbs"] > 1000
     assert bench.FFMA_PEAK_TFLOPS == pytest.approx(152 * 128 * 2 * 2.07 / 1e3)
+    tf, how = bench.ffma_peak(152, 2070.0)
+    assert tf == pytest.approx(80.55, abs=0.01) and "queried" in how
+    tf, how = bench.ffma_peak(None, None)  # nothing queried: GB300's figures
+    assert tf == pytest.approx(bench.FFMA_PEAK_TFLOPS) and "assumed" in how
+    assert bench.ffma_peak(148, 1965.0)[0] == pytest.approx(148 * 128 * 2 * 1.965 / 1e3)
 
 
 def test_traffic_entry_needs_matching_source(tmp_path, monkeypatch):

@@ -48,7 +48,8 @@ def test_enums_match_header():
                  "GEMM_OPT_WAIT_LIMIT_NS", "GEMM_OPT_TC_CTA_GROUP", "GEMM_OPT_TC_FAULT_INJECT",
                  "GEMM_OPT_SIMT_CONFIG", "GEMM_OPT_SIMT_TRANSPOSE", "GEMM_OPT_TC_STORE",
                  "GEMM_OPT_TC_MULTICAST", "GEMM_OPT_SOFTMAX_FAULT_INJECT",
-                 "GEMM_OPT_SIMT_SPLIT_TAIL", "GEMM_OPT_TC_SCHEDULER", "GEMM_ACT_NONE",
+                 "GEMM_OPT_SIMT_SPLIT_TAIL", "GEMM_OPT_TC_SCHEDULER",
+                 "GEMM_OPT_SIMT_FAULT_INJECT", "GEMM_ACT_NONE",
                  "GEMM_ACT_RELU", "GEMM_ACT_GELU"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m, name
@@ -147,8 +148,8 @@ def test_strerror_and_options(lib):
     assert lg.gemm_get_option(lg.GEMM_OPT_TC_CTA_GROUP) == 0
     assert lg.gemm_get_option(lg.GEMM_OPT_TC_FAULT_INJECT) == 0
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_CONFIG) == 0
-    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 9) == lg.GEMM_ERR_INVALID_ARG
-    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 8) == 0
+    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 10) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 9) == 0
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 0) == 0
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_TRANSPOSE) == 0
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_TRANSPOSE, 3) == lg.GEMM_ERR_INVALID_ARG
@@ -165,6 +166,8 @@ def test_strerror_and_options(lib):
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 0) == 0
     assert lg.gemm_get_option(lg.GEMM_OPT_TC_SCHEDULER) == 0
     assert lg.gemm_set_option(lg.GEMM_OPT_TC_SCHEDULER, 3) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_FAULT_INJECT) == 0
+    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_FAULT_INJECT, 2) == lg.GEMM_ERR_INVALID_ARG
 
 
 def test_launch_count_unchanged_by_rejected_calls(lib):

@@ -160,7 +160,7 @@ def test_k_one(dtype):
     run_and_check(129, 257, 1, dtype, 1, 0, 1, dist="int", seed=2)
 
 
-@pytest.mark.parametrize("config", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("config", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 @pytest.mark.parametrize("am,bm", list(itertools.product((0, 1), (0, 1))))
 def test_sgemm_every_tile_config(config, am, bm):
     old = lg.gemm_get_option(lg.GEMM_OPT_SIMT_CONFIG)
@@ -189,7 +189,7 @@ def test_sgemm_with_and_without_operand_transpose(transpose, am, bm, cm):
 # K-split of the FFMA kernel's last wave (GEMM_OPT_SIMT_SPLIT_TAIL): forced on
 # small and ragged shapes (every tile split, slices of one k-tile or empty),
 # and the automatic rule on a shape whose last wave is nearly empty.
-@pytest.mark.parametrize("config", [1, 5, 7])
+@pytest.mark.parametrize("config", [1, 5, 7, 9])
 @pytest.mark.parametrize("am,bm,cm", list(itertools.product((0, 1), (0, 1), (0, 1))))
 def test_sgemm_split_tail_forced(config, am, bm, cm):
     old = {o: lg.gemm_get_option(o) for o in (lg.GEMM_OPT_SIMT_SPLIT_TAIL,
@@ -204,6 +204,67 @@ def test_sgemm_split_tail_forced(config, am, bm, cm):
     finally:
         for o, v in old.items():
             lg.gemm_set_option(o, v)
+
+
+# Configuration 9 fills shared memory with TMA tensor copies when both
+# operands are MN-major with 16-byte aligned pitches (the pitch of n fp32
+# elements padded to a multiple of 4 here); shapes leave ragged M, N and K
+# (K below one 16-deep k-tile, and long enough to wrap the 5-stage ring many
+# times), and both C layouts swap which operand is A.
+def pad4(n: int) -> int:
+    return (-n) % 4
+
+
+def with_options(opts: dict, fn):
+    old = {o: lg.gemm_get_option(o) for o in opts}
+    for o, v in opts.items():
+        lg.check(lg.gemm_set_option(o, v))
+    try:
+        fn()
+    finally:
+        for o, v in old.items():
+            lg.gemm_set_option(o, v)
+
+
+TMA_SHAPES = [(4, 4, 1), (128, 128, 16), (130, 257, 7), (261, 132, 95), (516, 389, 333),
+              (1000, 1003, 1100)]
+
+
+@pytest.mark.parametrize("shape", TMA_SHAPES)
+@pytest.mark.parametrize("cm", (0, 1))
+def test_sgemm_tma_fed(shape, cm):
+    M, N, K = shape
+
+    def body():
+        run_and_check(M, N, K, lg.GEMM_F32, 1, 1, cm, dist="pm1", seed=M + K,
+                      lda_pad=pad4(M), ldb_pad=pad4(N) + 4)
+        run_and_check(M, N, K, lg.GEMM_F32, 1, 1, cm, dist="int", seed=M + N,
+                      lda_pad=pad4(M) + 8, ldb_pad=pad4(N), ldc_pad=1)
+    with_options({lg.GEMM_OPT_SIMT_CONFIG: 9}, body)
+
+
+@pytest.mark.parametrize("am,bm,cm", [(0, 0, 1), (0, 1, 0), (1, 0, 1), (0, 0, 0)])
+def test_sgemm_tma_fed_after_transpose(am, bm, cm):
+    # K-major operands reach the TMA path through the transpose pre-pass
+    # (MN-major copies with pitches rounded up to 4 elements)
+    def body():
+        run_and_check(301, 163, 97, lg.GEMM_F32, am, bm, cm, dist="pm1", seed=51,
+                      lda_pad=3, ldb_pad=1, ldc_pad=2)
+        run_and_check(64, 96, 33, lg.GEMM_F32, am, bm, cm, dist="int", seed=52)
+    with_options({lg.GEMM_OPT_SIMT_CONFIG: 9, lg.GEMM_OPT_SIMT_TRANSPOSE: 2}, body)
+
+
+@pytest.mark.parametrize("cm", (0, 1))
+def test_sgemm_tma_fed_split_tail_forced(cm):
+    # every last-wave tile cut into K-slices: slices of one k-tile, and empty
+    # slices (no copies, no waits) on the shortest K
+    def body():
+        for i, (M, N, K) in enumerate([(4, 4, 1), (16, 20, 7), (132, 260, 300),
+                                       (260, 132, 33)]):
+            run_and_check(M, N, K, lg.GEMM_F32, 1, 1, cm, dist="int", seed=60 + i,
+                          lda_pad=pad4(M), ldb_pad=pad4(N), ldc_pad=i % 3)
+        run_and_check(300, 520, 200, lg.GEMM_F32, 1, 1, cm, dist="pm1", seed=65)
+    with_options({lg.GEMM_OPT_SIMT_CONFIG: 9, lg.GEMM_OPT_SIMT_SPLIT_TAIL: 2}, body)
 
 
 @pytest.mark.parametrize("M,N,K", [(2557, 2043, 1100), (1000, 1001, 1100)])

@@ -121,3 +121,15 @@ def test_gemm_ex_with_split_tail(act):
         run_ex(130, 77, 40, lg.GEMM_F32, 1, 0, 0, act, -1.0, 0.0, False, seed=32)
     finally:
         lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, old)
+
+
+@pytest.mark.parametrize("act", sorted(ACTS))
+def test_gemm_ex_tma_fed_ffma(act):
+    # FFMA configuration 9 (TMA-fed, MN-major operands with 16-byte pitches)
+    old = lg.gemm_get_option(lg.GEMM_OPT_SIMT_CONFIG)
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 9))
+    try:
+        run_ex(300, 520, 200, lg.GEMM_F32, 1, 1, 1, act, 0.5, 0.25, True, seed=33)
+        run_ex(132, 260, 77, lg.GEMM_F32, 1, 1, 0, act, -1.0, 0.0, False, seed=34, ldc_pad=3)
+    finally:
+        lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, old)

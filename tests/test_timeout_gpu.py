@@ -60,6 +60,37 @@ def test_stalled_wait_times_out_and_device_recovers(cta_group, scheduler):
                    what=f"after timeout (cg={cta_group})")
 
 
+def test_stalled_ffma_tma_wait_times_out_and_device_recovers():
+    # FFMA configuration 9: with GEMM_OPT_SIMT_FAULT_INJECT the first CTA
+    # never loads its second k-tile, so its waits for that tile run out
+    import torch
+    M, N, K = 512, 512, 256
+    dA = torch.zeros(K * M, dtype=torch.float32, device="cuda")
+    dB = torch.zeros(K * N, dtype=torch.float32, device="cuda")
+    dC = torch.zeros(M * N, dtype=torch.float32, device="cuda")
+    assert lg.gemm_check_device_error() == lg.GEMM_OK
+    saved = {o: lg.gemm_get_option(o) for o in (lg.GEMM_OPT_WAIT_LIMIT_NS,
+                                                lg.GEMM_OPT_SIMT_FAULT_INJECT,
+                                                lg.GEMM_OPT_SIMT_CONFIG)}
+    try:
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_WAIT_LIMIT_NS, 20_000_000))
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 9))
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_FAULT_INJECT, 1))
+        rc = lg.gemm(M, N, K, dA, M, 1, dB, N, 1, dC, N, 1, lg.GEMM_F32)
+        assert rc == lg.GEMM_OK  # asynchronous: the timeout is reported later
+        assert lg.gemm_check_device_error() == lg.GEMM_ERR_TIMEOUT
+        assert lg.gemm_check_device_error() == lg.GEMM_OK
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_FAULT_INJECT, 0))
+        # the context is intact: the same kernel is exact again
+        A, lda, B, ldb = make_operands(300, 520, 200, lg.GEMM_F32, 1, 1, "int", 4)
+        C = run_device_gemm(300, 520, 200, lg.GEMM_F32, A, lda, 1, B, ldb, 1)
+        check_full(C, 300, 520, 200, lg.GEMM_F32, A, lda, 1, B, ldb, 1, exact=True,
+                   what="FFMA configuration 9 after a timeout")
+    finally:
+        for o, v in saved.items():
+            lg.gemm_set_option(o, v)
+
+
 def test_withheld_softmax_partial_times_out_and_device_recovers():
     import torch
     M, N = 6, 65536  # aligned rows of 65536 columns: clusters of 4 CTAs

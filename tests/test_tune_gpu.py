@@ -23,8 +23,8 @@ def _lib():
 
 
 @pytest.mark.parametrize("dtype,am,bm,cm,ldc_pad,expect", [
-    (lg.GEMM_F32, 0, 0, 1, 0, 16),        # 8 tile configs x {as is, transposed}
-    (lg.GEMM_F32, 1, 1, 1, 0, 8),         # MN-major operands: nothing to transpose
+    (lg.GEMM_F32, 0, 0, 1, 0, 18),        # 9 tile configs x {as is, transposed}
+    (lg.GEMM_F32, 1, 1, 1, 0, 9),         # MN-major operands: nothing to transpose
     (lg.GEMM_BF16_BF16, 0, 1, 1, 0, 10),  # 5 CTA modes / schedulers x 2 store paths
     (lg.GEMM_F16_F32, 1, 0, 0, 1, 5),     # misaligned C: st.global only
 ])
@@ -39,7 +39,7 @@ def test_tune_records_a_valid_choice(dtype, am, bm, cm, ldc_pad, expect):
                          iterations=2)
     assert rc == lg.GEMM_OK and t["candidates"] == expect and t["ms"] > 0
     if dtype == lg.GEMM_F32:
-        assert 1 <= t["simt_config"] <= 8 and t["simt_transpose"] in (1, 2)
+        assert 1 <= t["simt_config"] <= 9 and t["simt_transpose"] in (1, 2)
     else:
         assert (t["tc_cta_group"], t["tc_multicast"], t["tc_scheduler"]) in (
             (1, 1, 1), (1, 1, 2), (2, 1, 1), (2, 1, 2), (2, 2, 1))
