@@ -6,13 +6,18 @@
 //
 //   * one thread (thread 0) issues two 2-D tensor copies per k-tile (A and B
 //     boxes of 128 x 16 fp32, rows of 512 bytes, zero fill past M, N and K)
-//     that complete on the stage's `full` mbarrier;
+//     into a 6-stage ring; they complete on the stage's `full` mbarrier;
 //   * every thread arrives on the stage's `empty` mbarrier once it has read
-//     the stage; thread 0 waits for that before refilling it, and refills
-//     the stage read two k-tiles earlier, so the one warp that hosts the
-//     producer does not wait for the slowest warp on the tile just read;
+//     the stage; thread 0 waits for that before refilling it. While the CTA
+//     reads k-tile kt, thread 0 loads k-tile kt + 3 into the stage of
+//     k-tile kt - 3: three tiles are in flight ahead, and the two stages in
+//     between leave slack, so the warp that hosts the producer rarely waits
+//     for the slowest warp;
 //   * there is no CTA-wide barrier in the main loop: each warp only waits for
-//     its data, so the four warps of a CTA may drift apart by up to a stage;
+//     its data, so the four warps of a CTA may drift apart by up to two
+//     k-tiles (measured at 8192^3: 5 stages with one of slack ran 0.8%
+//     slower, 7 stages with two or three 1.5% slower, 12 stages of 8-deep
+//     k-tiles 7% slower, three CTAs per SM, which spills, 1.5% slower);
 //   * every wait is bounded (GEMM_OPT_WAIT_LIMIT_NS): one that runs out
 //     records a timeout in the device error word and the thread stops; thread
 //     0 then lets its copies in flight land (bounded) before the CTA exits.
@@ -28,15 +33,21 @@ namespace {
 
 using namespace gemm_ptx;
 
-using Cfg9 = SgCfg<16, 5, true, 2, 16>;  // k-depth 16, 5 stages, 8 x 16 per thread
 using Cfg7 = SgCfg<16, 4, true, 2, 16>;  // the cp.async fallback
 
-constexpr int kTmaBK = Cfg9::BK;
-constexpr int kTmaStages = Cfg9::STAGES;
-constexpr int kTileFloats = kTmaBK * BM;                     // one operand's k-tile, dense rows
-constexpr uint32_t kStageBytes = 2u * kTileFloats * 4u;      // A and B
-constexpr uint32_t kTxBytes = kStageBytes;                   // bytes a full stage receives
-constexpr int kTmaSmem = kTmaStages * (int)kStageBytes + 2 * kTmaStages * 8 + 1024;
+// A TMA-fed configuration: the tile shape of Cfg, LAG stages of slack
+// before a stage is refilled.
+template <class Cfg_, int LAG_>
+struct TmaCfg {
+    using Cfg = Cfg_;
+    static constexpr int LAG = LAG_;
+    static constexpr int BK = Cfg::BK;
+    static constexpr int STAGES = Cfg::STAGES;
+    static constexpr int TILE_FLOATS = BK * BM;                 // one operand's k-tile
+    static constexpr uint32_t STAGE_BYTES = 2u * TILE_FLOATS * 4u;  // A and B
+    static constexpr int SMEM = STAGES * (int)STAGE_BYTES + 2 * STAGES * 8 + 128;
+    static_assert(STAGES - 1 - LAG >= 1, "at least one k-tile in flight ahead");
+};
 
 struct TmaArgs {
     unsigned int* err;         // device error word
@@ -70,32 +81,37 @@ __device__ __forceinline__ bool sg_wait(uint32_t bar, uint32_t parity, const Tma
 // After a failed wait: thread 0 waits (bounded, ignoring the error word) for
 // the copies of k-tiles [from, to) it issued, so none lands after the CTA
 // has exited.
-__device__ __noinline__ void sg_drain(uint32_t full0, int from, int to, int skipped,
+__device__ __noinline__ void sg_drain(uint32_t full0, int stages, int from, int to, int skipped,
                                       unsigned long long limit) {
     const uint64_t t0 = globaltimer_ns();
     for (int j = from; j < to; ++j) {
         if (j == skipped) continue;  // never issued (test hook)
-        const uint32_t bar = full0 + 8u * (uint32_t)(j % kTmaStages);
-        const uint32_t par = (uint32_t)(j / kTmaStages) & 1u;
+        const uint32_t bar = full0 + 8u * (uint32_t)(j % stages);
+        const uint32_t par = (uint32_t)(j / stages) & 1u;
         while (!mbar_try_wait(bar, par))
             if (globaltimer_ns() - t0 > limit) return;
     }
 }
 
-__global__ void __launch_bounds__(Cfg9::THREADS, Cfg9::MINB)
+template <class TC>
+__global__ void __launch_bounds__(TC::Cfg::THREADS, TC::Cfg::MINB)
     sgemm_ffma_tma_kernel(const SgemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b, const TmaArgs x) {
-    constexpr int TN = Cfg9::TN;
+    using Cfg = typename TC::Cfg;
+    constexpr int TN = Cfg::TN;
     constexpr int NB = TN / 4;           // 4-column groups per thread
     constexpr int CSTEP = BN / NB / 4;   // float4s between a thread's groups
-    constexpr int S = kTmaStages;
-    constexpr int LAG = 1;               // stages of slack before a refill
+    constexpr int S = TC::STAGES;
+    constexpr int LAG = TC::LAG;         // stages of slack before a refill
+    constexpr int kTmaBK = TC::BK;
+    constexpr int kTileFloats = TC::TILE_FLOATS;
+    constexpr uint32_t kStageBytes = TC::STAGE_BYTES;
     extern __shared__ unsigned char smem_raw[];
     const int tid = threadIdx.x;
 
-    // 1024-byte aligned ring, then the full and empty barriers.
+    // 128-byte aligned ring, then the full and empty barriers.
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t base = (raw + 127u) & ~127u;
     const float* ring = reinterpret_cast<const float*>(smem_raw + (base - raw));
     const uint32_t full0 = base + S * kStageBytes, empty0 = full0 + 8u * S;
 
@@ -118,7 +134,7 @@ __global__ void __launch_bounds__(Cfg9::THREADS, Cfg9::MINB)
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, Cfg9::THREADS);
+            mbar_init(empty0 + 8u * s, Cfg::THREADS);
         }
         fence_mbarrier_init_cluster();
         fence_proxy_async_smem();
@@ -133,7 +149,7 @@ __global__ void __launch_bounds__(Cfg9::THREADS, Cfg9::MINB)
         const uint32_t bar = full0 + 8u * s;
         const uint32_t dst = base + s * kStageBytes;
         const int k = (kt0 + j) * kTmaBK;
-        mbar_arrive_expect_tx(bar, kTxBytes);
+        mbar_arrive_expect_tx(bar, kStageBytes);
         tma_load_2d<1>(dst, &tmap_a, bar, m0, k);
         tma_load_2d<1>(dst + (uint32_t)kTileFloats * 4u, &tmap_b, bar, n0, k);
     };
@@ -196,7 +212,7 @@ __global__ void __launch_bounds__(Cfg9::THREADS, Cfg9::MINB)
     }
     if (!ok) {
         // Thread 0's copies of k-tiles it has issued but not seen land.
-        if (tid == 0) sg_drain(full0, kt, issued, skip_tile1 ? 1 : -1, x.limit);
+        if (tid == 0) sg_drain(full0, S, kt, issued, skip_tile1 ? 1 : -1, x.limit);
         return;
     }
 
@@ -207,7 +223,7 @@ __global__ void __launch_bounds__(Cfg9::THREADS, Cfg9::MINB)
         for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int h = 0; h < NB; ++h)
-                wsp[(NB * i + h) * Cfg9::THREADS] =
+                wsp[(NB * i + h) * Cfg::THREADS] =
                     make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                                 acc[i][2 * h + 1].y);
         return;
@@ -215,16 +231,18 @@ __global__ void __launch_bounds__(Cfg9::THREADS, Cfg9::MINB)
     store_block<TN>(p, acc, m0, n0, ty, tx);
 }
 
+template <class TC>
 int launch_tma(SgemmParams sp, const DeviceInfo& dev, int split_mode, Scratch* scratch,
                uint64_t wait_limit_ns, int fault_inject, cudaStream_t stream) {
+    using Cfg = typename TC::Cfg;
+    auto kern = sgemm_ffma_tma_kernel<TC>;
     static std::atomic<uint64_t> configured{0};
     static std::atomic<int> per_sm[64];
     const int device = dev.device;
-    if (!configure_once(sgemm_ffma_tma_kernel, configured, device, kTmaSmem)) return kCuda;
+    if (!configure_once(kern, configured, device, TC::SMEM)) return kCuda;
     int occ = per_sm[device & 63].load();
     if (occ == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sgemm_ffma_tma_kernel,
-                                                          Cfg9::THREADS, kTmaSmem) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::THREADS, TC::SMEM) !=
             cudaSuccess) {
             cudaGetLastError();
             occ = -1;
@@ -234,12 +252,12 @@ int launch_tma(SgemmParams sp, const DeviceInfo& dev, int split_mode, Scratch* s
     alignas(64) CUtensorMap ta, tb;
     // A: M x K MN-major = K rows of M contiguous floats; box 128 (M) x 16 (K).
     if (!encode_tma_f32_2d(&ta, sp.A, (uint64_t)sp.M, (uint64_t)sp.K, (uint64_t)sp.lda, BM,
-                           kTmaBK) ||
+                           TC::BK) ||
         !encode_tma_f32_2d(&tb, sp.B, (uint64_t)sp.N, (uint64_t)sp.K, (uint64_t)sp.ldb, BN,
-                           kTmaBK))
+                           TC::BK))
         return kCuda;
     plan_split(sp, occ > 0 ? occ * dev.sm_count : 0, dev.sm_count,
-               (sp.K + kTmaBK - 1) / kTmaBK, split_mode);
+               (sp.K + TC::BK - 1) / TC::BK, split_mode);
     const int64_t tail = (int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles;
     if (tail > 0) {
         const size_t bytes = (size_t)tail * sp.splits * BM * BN * sizeof(float);
@@ -252,14 +270,13 @@ int launch_tma(SgemmParams sp, const DeviceInfo& dev, int split_mode, Scratch* s
     const TmaArgs x{dev.err_word, (unsigned long long)wait_limit_ns, fault_inject};
     const int64_t units =
         sp.dp_tiles + ((int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles) * sp.splits;
-    sgemm_ffma_tma_kernel<<<dim3((unsigned)units), dim3(Cfg9::THREADS), kTmaSmem, stream>>>(
-        sp, ta, tb, x);
+    kern<<<dim3((unsigned)units), dim3(Cfg::THREADS), TC::SMEM, stream>>>(sp, ta, tb, x);
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     note_launch();
     const int64_t fix = (int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles;
     if (fix > 0) {
-        sgemm_split_fixup_kernel<Cfg9::TN>
-            <<<dim3((unsigned)fix), dim3(Cfg9::THREADS), 0, stream>>>(sp);
+        sgemm_split_fixup_kernel<Cfg::TN>
+            <<<dim3((unsigned)fix), dim3(Cfg::THREADS), 0, stream>>>(sp);
         if (cudaGetLastError() != cudaSuccess) return kCuda;
         note_launch();
     }
@@ -272,7 +289,8 @@ int launch_sgemm_cfg9(const SgemmParams& sp, int av, int bv, const DeviceInfo& d
                       int split_mode, Scratch* scratch, uint64_t wait_limit_ns, int fault_inject,
                       cudaStream_t s) {
     if (av == 4 && bv == 4)
-        return launch_tma(sp, dev, split_mode, scratch, wait_limit_ns, fault_inject, s);
+        return launch_tma<TmaCfg<SgCfg<16, 6, true, 2, 16>, 2>>(sp, dev, split_mode, scratch,
+                                                                wait_limit_ns, fault_inject, s);
     return launch_layout<Cfg7>(sp, av, bv, dev.device, dev.sm_count, split_mode, scratch, s);
 }
 

@@ -299,7 +299,7 @@ enum gemm_option {
        Ampere example's 128 x 128 x 8 with 3 stages --,
        5 = (16, 4, packed, 1, 8 x 8), 6 = (32, 4, packed, 1, 8 x 8),
        7 = (16, 4, packed, 2, 8 x 16), 8 = (32, 3, packed, 2, 8 x 16),
-       9 = (16, 5, packed, 2, 8 x 16) with shared memory filled by TMA
+       9 = (16, 6, packed, 2, 8 x 16) with shared memory filled by TMA
        tensor copies and per-stage mbarriers instead of cp.async and a CTA
        barrier, when A and B (after any transpose) are MN-major with 16-byte
        aligned bases and row pitches; 7 otherwise.
