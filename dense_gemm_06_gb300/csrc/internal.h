@@ -42,8 +42,6 @@ struct DeviceInfo {
 
 // Launchers return 0 or a gemm_status. They enqueue exactly the kernels they
 // report through note_launch().
-// config: 0 = default tile configuration, 1..4 = a fixed one (see
-// GEMM_OPT_SIMT_CONFIG in gemm.h).
 // Stream-ordered scratch for one launch sequence: get() allocates once from
 // the pool; the caller frees `ptr` on the stream after the launches.
 struct Scratch {
@@ -58,8 +56,10 @@ struct Scratch {
         return ptr;
     }
 };
-// split_mode: 0 automatic (K-split the last wave's tiles when it is at most
-// half full), 1 never, 2 always split the last wave (tests).
+// config: the FFMA tile configuration, 1..9 (GEMM_OPT_SIMT_CONFIG in gemm.h).
+// split_mode: 0 automatic (K-split the tiles after the last full round of
+// tiles over the SMs when a per-SM model predicts >= 10% saved; plan_split in
+// sgemm_ffma.cu), 1 never, 2 always split the last wave (tests).
 // wait_limit_ns / fault_inject: the bounded mbarrier waits of configuration 9
 // (TMA-fed) and its test hook (1 = the first CTA never loads its second
 // k-tile, so its waits run out and report a timeout in the error word).

@@ -329,13 +329,16 @@ enum gemm_option {
        report GEMM_ERR_TIMEOUT through gemm_check_device_error; the row's y
        is then undefined. 0 (default) = off. */
     GEMM_OPT_SOFTMAX_FAULT_INJECT = 8,
-    /* Wave tail of the fp32 FFMA kernel: 0 = automatic (when the last wave of
-       128 x 128 tiles would fill at most half of the resident CTA slots, its
-       tiles are split along K into 2-4 slices computed by separate CTAs into
-       pool scratch and summed in slice order by a fixup kernel before the
-       epilogue), 1 = never split, 2 = always split the last wave (every tile
-       when there is less than one wave). A split changes the order of the
-       k-sum, never the per-product rounding. */
+    /* Wave tail of the fp32 FFMA kernel: 0 = automatic (the tiles left over
+       after the last full round of 128 x 128 tiles over the SMs are split
+       along K into 2-8 slices, computed by separate CTAs into pool scratch
+       and summed in slice order by a fixup kernel before the epilogue, when
+       a per-SM model predicts a saving of at least 10%, every slice keeps at
+       least 32 k-tiles, and there is no full round or at least two),
+       1 = never split, 2 = always split the last wave of resident CTAs into
+       2-4 slices (every tile when there is less than one wave; tests). A
+       split changes the order of the k-sum, never the per-product
+       rounding. */
     GEMM_OPT_SIMT_SPLIT_TAIL = 9,
     /* Tile scheduler of the tensor-core kernel (the Gluon Multi-CTA
        tutorial's CLC-scheduled matmul): 0 = automatic (currently static),
