@@ -298,18 +298,32 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
             }
         }
     } else {
+        // Lane = column; one coalesced row segment per store. The shared
+        // loads of RB rows are issued together before their stores, so their
+        // latencies overlap instead of adding up row by row.
+        constexpr int RB = 8;
         const int col = col0 + lane;
+        const bool col_ok = col < p.N;
         const int u = lane / PER_UNIT, e = lane % PER_UNIT;
-#pragma unroll 4
-        for (int r = 0; r < 32; ++r) {
-            const uint32_t a = stage + (uint32_t)(r * ROW_BYTES) +
-                               (uint32_t)((u ^ swz<ES>(r)) * 16) + (uint32_t)(e * ES);
-            if (row0 + r < p.M && col < p.N) {
-                OutT* dst = static_cast<OutT*>(p.C) + (int64_t)(row0 + r) * p.ldc + col;
-                if constexpr (ES == 4)
-                    *reinterpret_cast<uint32_t*>(dst) = lds32(a);
-                else
-                    *reinterpret_cast<uint16_t*>(dst) = lds16(a);
+#pragma unroll 1
+        for (int rb = 0; rb < 32; rb += RB) {
+            uint32_t val[RB];
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const int r = rb + i;
+                const uint32_t a = stage + (uint32_t)(r * ROW_BYTES) +
+                                   (uint32_t)((u ^ swz<ES>(r)) * 16) + (uint32_t)(e * ES);
+                if constexpr (ES == 4) val[i] = lds32(a);
+                else val[i] = lds16(a);
+            }
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const int r = rb + i;
+                if (row0 + r < p.M && col_ok) {
+                    OutT* dst = static_cast<OutT*>(p.C) + (int64_t)(row0 + r) * p.ldc + col;
+                    if constexpr (ES == 4) *reinterpret_cast<uint32_t*>(dst) = val[i];
+                    else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)val[i];
+                }
             }
         }
     }
