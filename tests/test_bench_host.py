@@ -114,3 +114,26 @@ def test_traffic_entry_needs_matching_source(tmp_path, monkeypatch):
     (src_dir / "k.cu").write_text("// kernel v2\n")
     assert bench.profiled_traffic("k") is None
     assert bench.profiled_traffic("missing") is None
+
+
+def test_traffic_entry_over_several_sources(tmp_path, monkeypatch):
+    # a kernel spread over several files is keyed on all of them, in order
+    import hashlib
+    src_dir = tmp_path / "dense_gemm_06_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (src_dir / "k.cuh").write_text("// kernel\n")
+    (src_dir / "helpers.cuh").write_text("// helpers v1\n")
+    digest = hashlib.sha256(b"// kernel\n// helpers v1\n").hexdigest()[:16]
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    entry = {"bytes_per_launch": 456, "source": ["k.cuh", "helpers.cuh"],
+             "source_sha256_16": digest}
+    (prof / "traffic.json").write_text(json.dumps({"k": entry}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("k") == 456
+    (src_dir / "helpers.cuh").write_text("// helpers v2\n")  # either file changing
+    assert bench.profiled_traffic("k") is None
+    (src_dir / "helpers.cuh").write_text("// helpers v1\n")
+    (src_dir / "k.cuh").unlink()                              # or going missing
+    assert bench.profiled_traffic("k") is None
+
