@@ -20,6 +20,7 @@
 #include "../../include/gemm.h"
 #include "epilogue.cuh"
 #include "internal.h"
+#include "policy.h"
 
 namespace libgemm {
 
@@ -280,18 +281,6 @@ Problem normalise(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, i
     return p;
 }
 
-// Whether to give the FFMA kernel an MN-major copy of a K-major operand.
-// The kernel reads MN-major tiles with 16-byte copies and K-major ones with
-// transposing 4-byte copies (about 10% slower at 8192^3); a transpose costs
-// two HBM passes over the operand, 48/n of the GEMM time for the other
-// dimension n, so it pays when n >= 512 and the product is large enough for
-// the extra launch not to matter.
-bool want_transpose(int64_t other_dim, const Problem& p, int mode) {
-    if (mode == 1) return false;
-    if (mode == 2) return true;
-    return other_dim >= 512 && (double)p.M * (double)p.N * (double)p.K >= 2147483648.0;
-}
-
 int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunConfig& cfg,
               cudaStream_t s) {
     void* scratch[2] = {nullptr, nullptr};
@@ -302,7 +291,7 @@ int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCon
     const int64_t rows[2] = {p.M, p.N};
     const int64_t other[2] = {p.N, p.M};
     for (int i = 0; i < 2 && rc == kOk; ++i) {
-        if (!*kmaj[i] || !want_transpose(other[i], p, cfg.simt_transpose)) continue;
+        if (!*kmaj[i] || !want_transpose(other[i], p.M, p.N, p.K, cfg.simt_transpose)) continue;
         const int64_t ld2 = round_up(rows[i], 4);  // 16-byte rows for vector copies
         if (cudaMallocFromPoolAsync(&scratch[i], (size_t)(p.K * ld2 * 4), pool, s) !=
             cudaSuccess) {
@@ -523,30 +512,6 @@ int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_m
     }
 }
 
-namespace {
-
-// Rows of the normalised C per gemm_host panel: a whole number of waves of
-// the kernel that computes it (so no panel adds a partial wave), at most
-// about 8 panels; M itself when the product is too small for overlapping the
-// copies with compute to pay.
-int64_t host_panel_rows(const Problem& p, const DeviceInfo& dev, const RunConfig& cfg) {
-    if (p.K == 0 || (double)p.M * (double)p.N * (double)p.K < 1.0e10) return p.M;
-    const bool f32 = p.dtype == GEMM_F32;
-    const bool one_cta = f32 || cfg.cta_group == 1;
-    const int64_t tm = f32 ? 128 : (cfg.cta_group == 1 ? 128 : (cfg.multicast == 2 ? 512 : 256));
-    const int64_t tn = f32 ? 128 : 256;
-    int64_t slots = f32 ? (int64_t)dev.sm_count * (cfg.simt_config == 5 || cfg.simt_config == 6
-                                                      ? 1 : 2)
-                        : (int64_t)dev.sm_count / (one_cta ? 1 : (cfg.multicast == 2 ? 4 : 2));
-    if (slots < 1) slots = 1;
-    const int64_t tiles_m = (p.M + tm - 1) / tm, tiles_n = (p.N + tn - 1) / tn;
-    int64_t r = slots / std::gcd(slots, tiles_n);
-    while (r * 8 < tiles_m) r *= 2;
-    return r >= tiles_m ? p.M : r * tm;
-}
-
-}  // namespace
-
 int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
               const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
               int dtype, void* stream) {
@@ -601,7 +566,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         // host_panel_rows gives at most about 8 panels; more than kMaxPanels
         // would only come from a model error, and then the call runs whole.
         constexpr int kMaxPanels = 64;
-        int64_t rows = host_panel_rows(pd, *dev, cfg);
+        // FFMA configurations 5 and 6 are sized for one CTA per SM, the others two
+        const int ctas_per_sm = cfg.simt_config == 5 || cfg.simt_config == 6 ? 1 : 2;
+        int64_t rows = host_panel_rows(pd.M, pd.N, pd.K, dtype == GEMM_F32, ctas_per_sm,
+                                       cfg.cta_group, cfg.multicast, dev->sm_count);
         if ((pd.M + rows - 1) / rows > kMaxPanels) rows = pd.M;
         const int np = (int)((pd.M + rows - 1) / rows);
 
@@ -650,7 +618,7 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         if (rc == kOk && np > 1 && K > 0 && dtype == GEMM_F32 && pd.b_kmajor) {
             Problem q0 = pd;
             q0.M = prow;
-            if (want_transpose(q0.M, q0, cfg.simt_transpose)) {
+            if (want_transpose(q0.M, q0.M, q0.N, q0.K, cfg.simt_transpose)) {
                 const int64_t ld2 = round_up(pd.N, 4);
                 if (cudaMallocFromPoolAsync(&bt, (size_t)(K * ld2 * 4), pool, s) != cudaSuccess) {
                     cudaGetLastError();

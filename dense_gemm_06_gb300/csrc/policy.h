@@ -1,0 +1,103 @@
+// policy.h -- the host-side choices the library makes automatically, as plain
+// C++ (no CUDA), so they can be compiled and checked on a machine without a
+// GPU: the FFMA kernel's K-split of the tiles left after its last full round,
+// whether a K-major fp32 operand is first transposed, and the row panels
+// gemm_host() pipelines its copies over.
+#pragma once
+
+#include <cstdint>
+#include <numeric>
+
+namespace libgemm {
+
+// K-split of the FFMA kernel's tail. Tiles 0 .. dp_tiles-1 (raster order) run
+// whole; every later tile is cut into `splits` K-slices of `kt_slice` k-tiles,
+// one CTA each, summed in slice order by a fixup kernel.
+struct TailSplit {
+    int dp_tiles;
+    int splits;
+    int kt_slice;
+};
+
+// Model: an SM finishes the same tile work per unit of time whether it holds
+// one CTA or two, so a launch takes (most tile-units on one SM) x (work of a
+// unit). With P SMs and T tiles, q = T / P full rounds and r = T mod P tail
+// tiles: whole, the tail adds one round; cut into s K-slices (one CTA each),
+// it adds ceil(r s / P) / s. split_mode 0 (automatic): with no full round (the
+// GPU under-filled) or at least two, the s in 2..8 (slices of at least 32
+// k-tiles: shorter ones spend too much of their time filling the pipeline
+// and writing partial sums) with the shortest time, if that saves at least
+// 10% against no split. With exactly one full round the model fails
+// (measured at 2048^3: 4 slices ran 12% slower than whole tiles), so that
+// case is not split. split_mode 1: never. split_mode 2 (tests): always cut
+// the last wave of `slots` resident CTAs (all tiles if T < slots) into 2-4
+// slices. slots <= 0 (occupancy unknown) or sm_count <= 0: never.
+inline TailSplit plan_tail_split(int64_t T, int slots, int sm_count, int nkt, int split_mode) {
+    TailSplit t{(int)T, 1, nkt};
+    if (split_mode == 1 || slots <= 0 || sm_count <= 0 || T <= 0) return t;
+    if (split_mode == 2) {
+        int64_t r = T % slots;
+        if (r == 0) r = T < slots ? T : slots;
+        int s = (int)(slots / r);
+        s = s < 2 ? 2 : (s > 4 ? 4 : s);
+        t.dp_tiles = (int)(T - r);
+        t.splits = s;
+        t.kt_slice = (nkt + s - 1) / s;
+        return t;
+    }
+    const int64_t P = sm_count, q = T / P, r = T % P;
+    if (r == 0 || q == 1) return t;
+    const double whole = (double)(q + 1);
+    double best = whole;
+    int best_s = 1;
+    for (int s = 2; s <= 8 && nkt >= 32 * s; ++s) {
+        const double time = (double)q + (double)((r * s + P - 1) / P) / s;
+        if (time < best - 1e-9) {
+            best = time;
+            best_s = s;
+        }
+    }
+    if (best_s == 1 || best > 0.9 * whole) return t;
+    t.dp_tiles = (int)(T - r);
+    t.splits = best_s;
+    t.kt_slice = (nkt + best_s - 1) / best_s;
+    return t;
+}
+
+// Whether to give the FFMA kernel an MN-major copy of a K-major operand.
+// The kernel reads MN-major tiles with 16-byte copies (or TMA) and K-major
+// ones with transposing 4-byte copies (about 10% slower at 8192^3); a
+// transpose costs two HBM passes over the operand, 48/n of the GEMM time for
+// the other dimension n, so it pays when n >= 512 and the product is large
+// enough for the extra launch not to matter. mode: 0 automatic, 1 never,
+// 2 always.
+inline bool want_transpose(int64_t other_dim, int64_t M, int64_t N, int64_t K, int mode) {
+    if (mode == 1) return false;
+    if (mode == 2) return true;
+    return other_dim >= 512 && (double)M * (double)N * (double)K >= 2147483648.0;
+}
+
+// Rows of the normalised C per gemm_host() panel: a whole number of waves of
+// the kernel that computes it (so no panel adds a partial wave), at most
+// about 8 panels; M itself when the product is too small (M N K < 1e10) for
+// overlapping the copies with compute to pay. f32: the FFMA kernel (128 x
+// 128 tiles, `ctas_per_sm` resident CTAs per SM); otherwise the tensor-core
+// kernel with CTA group `cta_group` (1: 128 x 256 tiles, one CTA each; 2:
+// 256 x 256 tiles per CTA pair) and operand multicast (2: clusters of two
+// pairs, 512 x 256).
+inline int64_t host_panel_rows(int64_t M, int64_t N, int64_t K, bool f32, int ctas_per_sm,
+                               int cta_group, int multicast, int sm_count) {
+    if (K == 0 || (double)M * (double)N * (double)K < 1.0e10) return M;
+    const bool one_cta = f32 || cta_group == 1;
+    const int64_t tm = f32 ? 128 : (cta_group == 1 ? 128 : (multicast == 2 ? 512 : 256));
+    const int64_t tn = f32 ? 128 : 256;
+    int64_t slots = f32 ? (int64_t)sm_count * ctas_per_sm
+                        : (int64_t)sm_count / (one_cta ? 1 : (multicast == 2 ? 4 : 2));
+    if (slots < 1) slots = 1;
+    const int64_t tiles_m = (M + tm - 1) / tm, tiles_n = (N + tn - 1) / tn;
+    int64_t r = slots / std::gcd(slots, tiles_n);
+    while (r * 8 < tiles_m) r *= 2;
+    return r >= tiles_m ? M : r * tm;
+}
+
+}  // namespace libgemm

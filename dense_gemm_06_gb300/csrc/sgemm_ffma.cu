@@ -29,6 +29,7 @@
 //     normal epilogue, so the last wave takes 1/splits of the time.
 #include <cstdint>
 
+#include "policy.h"
 #include "sgemm_ffma.cuh"
 
 namespace libgemm {
@@ -67,51 +68,14 @@ bool aligned16(const void* p, int64_t ld) {
 
 }  // namespace
 
-// Chooses the K-split of the tail tiles. Model: an SM finishes the same
-// tile work per unit of time whether it holds one CTA or two, so a launch
-// takes (most tile-units on one SM) x (work of a unit). With P SMs and T
-// tiles, q = T / P full rounds and r = T mod P tail tiles: whole, the tail
-// adds one round; cut into s K-slices (one CTA each), it adds
-// ceil(r s / P) / s. Automatic: with no full round (the GPU under-filled)
-// or at least two, the s in 2..8 (slices of at least 32 k-tiles: shorter
-// ones spend too much of their time filling the pipeline and writing
-// partial sums) with the shortest time, if that saves at least 10% against
-// no split. With exactly one full round the model fails (measured at 2048^3:
-// 4 slices ran 12% slower than whole tiles), so that case is not split. split_mode 2 (tests)
-// always cuts the last wave of `slots` CTAs (all tiles if T < slots) into
-// at least 2 slices.
+// Chooses the K-split of the tail tiles (the model is plan_tail_split's, in
+// policy.h).
 void plan_split(SgemmParams& sp, int slots, int sm_count, int nkt, int split_mode) {
-    const int64_t T = (int64_t)sp.tiles_m * sp.tiles_n;
-    sp.dp_tiles = (int)T;
-    sp.splits = 1;
-    sp.kt_slice = nkt;
-    if (split_mode == 1 || slots <= 0 || sm_count <= 0 || T <= 0) return;
-    if (split_mode == 2) {
-        int64_t r = T % slots;
-        if (r == 0) r = T < slots ? T : slots;
-        int s = (int)(slots / r);
-        s = s < 2 ? 2 : (s > 4 ? 4 : s);
-        sp.dp_tiles = (int)(T - r);
-        sp.splits = s;
-        sp.kt_slice = (nkt + s - 1) / s;
-        return;
-    }
-    const int64_t P = sm_count, q = T / P, r = T % P;
-    if (r == 0 || q == 1) return;
-    const double whole = (double)(q + 1);
-    double best = whole;
-    int best_s = 1;
-    for (int s = 2; s <= 8 && nkt >= 32 * s; ++s) {
-        const double t = (double)q + (double)((r * s + P - 1) / P) / s;
-        if (t < best - 1e-9) {
-            best = t;
-            best_s = s;
-        }
-    }
-    if (best_s == 1 || best > 0.9 * whole) return;
-    sp.dp_tiles = (int)(T - r);
-    sp.splits = best_s;
-    sp.kt_slice = (nkt + best_s - 1) / best_s;
+    const TailSplit t =
+        plan_tail_split((int64_t)sp.tiles_m * sp.tiles_n, slots, sm_count, nkt, split_mode);
+    sp.dp_tiles = t.dp_tiles;
+    sp.splits = t.splits;
+    sp.kt_slice = t.kt_slice;
 }
 
 int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,

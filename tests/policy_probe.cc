@@ -1,0 +1,39 @@
+// policy_probe.cc -- prints the library's automatic host-side choices for the
+// problems given on the command line, compiled with a plain C++ compiler
+// against the library's own policy header (tests/test_policy.py drives it).
+//
+//   split  T slots sm_count nkt mode      -> "dp_tiles splits kt_slice"
+//   transpose other M N K mode            -> "0" or "1"
+//   panel  M N K f32 ctas_per_sm cta_group multicast sm_count -> "rows"
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "policy.h"
+
+static long long arg(char** argv, int i) { return std::atoll(argv[i]); }
+
+int main(int argc, char** argv) {
+    using namespace libgemm;
+    if (argc >= 7 && std::strcmp(argv[1], "split") == 0) {
+        const TailSplit t = plan_tail_split(arg(argv, 2), (int)arg(argv, 3), (int)arg(argv, 4),
+                                            (int)arg(argv, 5), (int)arg(argv, 6));
+        std::printf("%d %d %d\n", t.dp_tiles, t.splits, t.kt_slice);
+        return 0;
+    }
+    if (argc >= 7 && std::strcmp(argv[1], "transpose") == 0) {
+        std::printf("%d\n", want_transpose(arg(argv, 2), arg(argv, 3), arg(argv, 4), arg(argv, 5),
+                                           (int)arg(argv, 6)) ? 1 : 0);
+        return 0;
+    }
+    if (argc >= 10 && std::strcmp(argv[1], "panel") == 0) {
+        std::printf("%lld\n",
+                    (long long)host_panel_rows(arg(argv, 2), arg(argv, 3), arg(argv, 4),
+                                               arg(argv, 5) != 0, (int)arg(argv, 6),
+                                               (int)arg(argv, 7), (int)arg(argv, 8),
+                                               (int)arg(argv, 9)));
+        return 0;
+    }
+    std::fprintf(stderr, "usage: see the header of policy_probe.cc\n");
+    return 2;
+}

@@ -1,0 +1,102 @@
+"""The library's automatic host-side choices, checked on the CPU: the FFMA
+kernel's K-split of the tiles after its last full round (the per-SM model),
+the transpose rule for K-major fp32 operands, and the row panels that
+gemm_host() pipelines its copies over. tests/policy_probe.cc is compiled with
+the host C++ compiler against the library's own policy header, so these are
+the choices the library makes; the expected values are the outcomes the
+model gives by hand for a 152-SM GB300 (two FFMA CTAs per SM), including the
+shapes whose splits were measured (2560x2048x8192: 8 slices;
+4096x2048x2048: 2; 1024x1024x8192: 7; 8192^3 and 2048^3: none)."""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(os.path.dirname(HERE), "dense_gemm_06_gb300", "csrc")
+P, SLOTS = 152, 304  # SMs, resident FFMA CTAs (two per SM)
+
+
+@pytest.fixture(scope="module")
+def probe(tmp_path_factory):
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no host C++ compiler")
+    exe = str(tmp_path_factory.mktemp("policy") / "policy_probe")
+    subprocess.run([cxx, "-std=c++17", "-O1", "-I", CSRC, os.path.join(HERE, "policy_probe.cc"),
+                    "-o", exe], check=True, capture_output=True, text=True)
+
+    def run(*args):
+        out = subprocess.run([exe, *map(str, args)], check=True, capture_output=True, text=True)
+        vals = [int(v) for v in out.stdout.split()]
+        return vals[0] if len(vals) == 1 else tuple(vals)
+    return run
+
+
+def tiles(M, N):
+    return ((M + 127) // 128) * ((N + 127) // 128)
+
+
+@pytest.mark.parametrize("M,N,K,want", [
+    # 320 tiles: 2 full rounds + 16; s in 2..8 adds 1/s of a round -> 8 slices
+    (2560, 2048, 8192, (304, 8, 64)),
+    # 512 tiles: 3 rounds + 56; 128 k-tiles allow s <= 4; s = 2 saves 12.5%
+    (4096, 2048, 2048, (456, 2, 64)),
+    # 64 tiles, no full round: 7 slices take 3/7 of a round
+    (1024, 1024, 8192, (0, 7, 74)),
+    # 4096 tiles: 26 rounds + 144 -- no split saves a round
+    (8192, 8192, 8192, (4096, 1, 512)),
+    # exactly one full round: the model does not hold there, never split
+    (2048, 2048, 2048, (256, 1, 128)),
+    # a whole number of rounds: nothing to split
+    (2432, 2048, 4096, (304, 1, 256)),
+    # 9 rounds + 100: even the best split saves less than 10%
+    (1468 * 128, 128, 8192, (1468, 1, 512)),
+    # 64 tiles but only 40 k-tiles: no slice would keep 32 k-tiles
+    (1024, 1024, 640, (64, 1, 40)),
+])
+def test_tail_split_automatic(probe, M, N, K, want):
+    assert probe("split", tiles(M, N), SLOTS, P, (K + 15) // 16, 0) == want
+
+
+def test_tail_split_never_and_forced(probe):
+    assert probe("split", 320, SLOTS, P, 512, 1) == (320, 1, 512)
+    # forced (tests): the last wave of resident CTAs in 2..4 slices
+    assert probe("split", 320, SLOTS, P, 512, 2) == (304, 4, 128)   # 16 tail tiles
+    assert probe("split", 64, SLOTS, P, 512, 2) == (0, 4, 128)      # under one wave
+    assert probe("split", 608, SLOTS, P, 512, 2) == (304, 2, 256)   # whole waves
+    assert probe("split", 1000, SLOTS, P, 7, 2) == (912, 3, 3)      # 88 tail tiles
+    # occupancy unknown: never
+    assert probe("split", 320, 0, P, 512, 0) == (320, 1, 512)
+    assert probe("split", 0, SLOTS, P, 512, 0) == (0, 1, 512)
+
+
+def test_transpose_rule(probe):
+    assert probe("transpose", 8192, 8192, 8192, 8192, 0) == 1
+    assert probe("transpose", 511, 8192, 511, 8192, 0) == 0      # other dimension < 512
+    assert probe("transpose", 1024, 1024, 1024, 2047, 0) == 0    # M N K just below 2^31
+    assert probe("transpose", 1024, 1024, 1024, 2048, 0) == 1    # M N K = 2^31
+    assert probe("transpose", 8192, 8192, 8192, 8192, 1) == 0    # never
+    assert probe("transpose", 4, 4, 4, 4, 2) == 1                # always
+
+
+def test_host_panels(probe):
+    # fp32 8192^3: 304 CTA slots, 64 tile columns -> 19 tile rows per panel
+    # (a whole number of waves), so 8192 rows go as 2432 x 3 + 896
+    assert probe("panel", 8192, 8192, 8192, 1, 2, 2, 1, P) == 2432
+    # bf16 8192^3 on 76 CTA pairs (256 x 256 tiles): 19 tile rows of 256
+    assert probe("panel", 8192, 8192, 8192, 0, 2, 2, 1, P) == 4864
+    # one CTA per 128 x 256 tile: 152 slots, 32 tile columns -> 19 rows of 128
+    assert probe("panel", 8192, 8192, 8192, 0, 2, 1, 1, P) == 2432
+    # clusters of two pairs (512-row tiles): 19 tile rows exceed the 16 there
+    assert probe("panel", 8192, 8192, 8192, 0, 2, 2, 2, P) == 8192
+    # the FFMA slots per SM matter: 18 tile columns, 304 vs 152 slots
+    assert probe("panel", 16384, 2304, 8192, 1, 2, 2, 1, P) == 16384
+    assert probe("panel", 16384, 2304, 8192, 1, 1, 2, 1, P) == 9728
+    # more than 8 panels' worth of waves: the wave count is doubled
+    assert probe("panel", 400000, 128, 1000, 1, 2, 2, 1, P) == 77824
+    # too small to pipeline (M N K < 1e10), or nothing to multiply
+    assert probe("panel", 2048, 2048, 2048, 1, 2, 2, 1, P) == 2048
+    assert probe("panel", 8192, 8192, 0, 1, 2, 2, 1, P) == 8192
