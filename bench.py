@@ -1,4 +1,4 @@
-"""Benchmark: GEMM TFLOP/s at 8192^3 on one GB300 (and N replicas).
+"""Benchmark: GEMM TFLOP/s at 8192^3 on one GB300.
 
 One step is one pass of the whole hot path over one batch of seeded
 synthetic inputs: the 8192^3 fp32 SGEMM on the FFMA kernel for each of the
@@ -7,15 +7,16 @@ four A/B major combinations (C N-major), then the 8192^3 bf16 -> bf16 GEMM
 Ampere SGEMM example's ncu recipe and the 8192 x 8192 x 8192 point of the
 Gluon Multi-CTA tutorial's matmul benchmark.
 
-    value        = 5 * 2 * 8192^3 * steps * n_gpus / (max over ranks of the
-                   device time of the timed steps), inputs resident in HBM
+    value        = 5 * 2 * 8192^3 * steps / (device time of the timed steps),
+                   inputs resident in HBM
     e2e          = the same through gemm_host(): pinned host A, B in, host C
                    out, copies inside the timed region
     roofline     = the dominant kernel (the FFMA SGEMM) against its ALU peak
     cpu_baseline = the fp64 CPU oracle on a bounded sample of the workload
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-Under torchrun every rank runs the same step on its own GPU (replicas).
+Usage: python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl native|reference]
+The library runs on one GPU (its opt-in cluster-multicast TMA variant must
+only ever address this GPU's memory), so --gpus accepts 1 only.
 """
 
 from __future__ import annotations
@@ -68,11 +69,6 @@ def load_peaks():
         return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
     except Exception:
         return dict(FALLBACK_PEAKS), "fallback"
-
-
-def dist_env():
-    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
-        int(os.environ.get("LOCAL_RANK", 0))
 
 
 # ------------------------------------------------------------- inputs --
@@ -159,10 +155,9 @@ def summarize_clocks(lines):
             "reasons": reasons, "samples": len(rows)}
 
 
-def throughput_tflops(flops_per_step, steps, world, ms):
-    """Whole-job TFLOP/s: every rank ran `steps` steps; `ms` is the slowest
-    rank's device time (weak scaling over replicas)."""
-    return flops_per_step * steps * world / (ms * 1e-3) / 1e12
+def throughput_tflops(flops_per_step, steps, ms):
+    """TFLOP/s of `steps` steps of `flops_per_step` that took `ms` of device time."""
+    return flops_per_step * steps / (ms * 1e-3) / 1e12
 
 
 # ------------------------------------------------------- native arm --
@@ -172,13 +167,9 @@ def run_native(args):
 
     import dense_gemm_06_gb300 as lg
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(0)
     lg.load()
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(device=dev)
     s_handle = stream.cuda_stream
 
@@ -214,9 +205,8 @@ def run_native(args):
     stream.synchronize()
     lg.check(lg.gemm_check_device_error(s_handle), "device error word")
 
-    barrier(world)
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(0)
     launches0 = lg.gemm_launch_count()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -226,29 +216,25 @@ def run_native(args):
     t_end.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
-    barrier(world)
     clocks = sampler.stop()
     launches = lg.gemm_launch_count() - launches0
     lg.check(lg.gemm_check_device_error(s_handle), "device error word")
 
     ms_total = t_start.elapsed_time(t_end)
-    ms_total = max_over_ranks(ms_total, world, dev)
     per = np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(n_gemms)]
                     for k in range(args.steps)])
     per_ms = per.mean(axis=0)
 
-    parity = sampled_parity(C16, C32, f32, bf, d, lg, s_handle) if rank == 0 else None
+    parity = sampled_parity(C16, C32, f32, bf, d, lg, s_handle)
 
     # e2e through the host-buffer entry point (pinned host memory)
-    e2e = run_e2e(args, lg, f32, bf, stream, world, dev)
+    e2e = run_e2e(args, lg, f32, bf, stream)
 
-    if rank != 0:
-        return
     peaks, peak_src = load_peaks()
     ffma_tf, ffma_how = ffma_peak(torch.cuda.get_device_properties(dev).multi_processor_count,
                                   (clocks or {}).get("sm_max_mhz"))
     flops_step = FLOPS_PER_GEMM * n_gemms
-    value = throughput_tflops(flops_step, args.steps, world, ms_total)
+    value = throughput_tflops(flops_step, args.steps, ms_total)
     parts = []
     for i, (name, am, bm) in enumerate(GEMMS):
         tf = FLOPS_PER_GEMM / (per_ms[i] * 1e-3) / 1e12
@@ -273,7 +259,7 @@ def run_native(args):
                    "traffic": profiled_traffic("gemm_tc_kernel"), "kernel": "gemm_tc_kernel",
                    "peak_source": f"MEASURED_PEAKS bf16_tflops burst ({peak_src})"}
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+bf16",
         "data": "synthetic: seeded SplitMix64 N(0,1), fp32 (seed 1027) and bf16 (seed 1028)",
@@ -281,7 +267,7 @@ def run_native(args):
                    "gemms_per_step": n_gemms,
                    "l2": "no flush; every operand (256 MiB fp32, 128 MiB bf16) exceeds the "
                          "129 MB L2 and a step streams >2 GB",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": "single GPU"},
         "roofline": roofline, "roofline_tc": roofline_tc, "parts": parts,
         "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks, "parity": parity,
         "cpu_baseline": cpu_baseline(f32, bf) if not args.no_cpu_baseline else None,
@@ -289,24 +275,7 @@ def run_native(args):
     print(json.dumps(line), flush=True)
 
 
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(x, world, dev):
-    """The largest `x` over all ranks (the job's time is the slowest rank's)."""
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def run_e2e(args, lg, f32, bf, stream, world, dev):
+def run_e2e(args, lg, f32, bf, stream):
     """The step through gemm_host(): pinned host operands in, host C out."""
     import torch
     n = NDIM
@@ -328,18 +297,16 @@ def run_e2e(args, lg, f32, bf, stream, world, dev):
     for _ in range(max(1, min(args.warmup, 2))):
         step()
     stream.synchronize()
-    barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(steps):
         step()
     e1.record(stream)
     stream.synchronize()
-    barrier(world)
-    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    ms = e0.elapsed_time(e1)
     h2d = 4 * 2 * n * n * 4 + 2 * n * n * 2
     d2h = 4 * n * n * 4 + n * n * 2
-    return {"value": round(throughput_tflops(FLOPS_PER_GEMM * 5, steps, world, ms), 3),
+    return {"value": round(throughput_tflops(FLOPS_PER_GEMM * 5, steps, ms), 3),
             "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(ms / steps, 3),
             "api": "gemm_host (C ABI, pinned host buffers)"}
@@ -475,9 +442,6 @@ def cpu_baseline(f32, bf):
 def run_reference(args):
     """The reference arm: the CPU oracle timed on this machine's host cores on the
     same workload, each step a bounded sample of it."""
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return
     import oracle
     f32, bf = make_inputs()
     rows = REF_ROWS
@@ -493,7 +457,7 @@ def run_reference(args):
               f"fp64 triple loop")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": NDIM, "N": NDIM, "K": NDIM,
@@ -507,7 +471,8 @@ def run_reference(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1, choices=[1],
+                    help="1 only: libgemm is a single-GPU library")
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")

@@ -28,8 +28,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Per-device error word written by kernels that give up on a wait.
-__device__ unsigned int g_err_word;
+// Per-device error word written by kernels that give up on a wait (the
+// largest generation of a launch whose wait ran out; see internal.h).
+__device__ ErrWord g_err_word;
+std::atomic<ErrWord> g_generation{1};
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
@@ -132,7 +134,7 @@ int current_device(DeviceInfo** out, cudaMemPool_t* pool) {
         st.info.sm_count = prop.multiProcessorCount;
         st.info.cc_major = prop.major;
         st.info.cc_minor = prop.minor;
-        st.info.err_word = static_cast<unsigned int*>(err);
+        st.info.err_word = static_cast<ErrWord*>(err);
         if (cudaStreamCreateWithFlags(&st.h2d, cudaStreamNonBlocking) != cudaSuccess ||
             cudaStreamCreateWithFlags(&st.d2h, cudaStreamNonBlocking) != cudaSuccess) {
             cudaGetLastError();
@@ -389,7 +391,7 @@ RunConfig resolve(const TuneKey& key) {
     if (c.simt_config == 0) c.simt_config = tuned && t.simt_config ? t.simt_config : 9;
     if (c.simt_transpose == 0 && tuned) c.simt_transpose = t.simt_transpose;
     if (c.cta_group == 0) c.cta_group = tuned && t.tc_cta_group ? t.tc_cta_group : 2;
-    if (c.multicast == 0) c.multicast = tuned && t.tc_multicast ? t.tc_multicast : 1;
+    c.multicast = c.multicast == 2 ? 2 : 1;  // only on request, never from a tuned entry
     if (c.tc_store == 0 && tuned) c.tc_store = t.tc_store;
     if (c.tc_scheduler == 0) c.tc_scheduler = tuned && t.tc_scheduler ? t.tc_scheduler : 1;
     return c;
@@ -442,13 +444,40 @@ Problem normalised(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     return normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
 }
 
-int error_word_address(unsigned int** out) {
+int error_word_address(ErrWord** out) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) {
         cudaGetLastError();
         return kCuda;
     }
-    *out = static_cast<unsigned int*>(p);
+    *out = static_cast<ErrWord*>(p);
+    return kOk;
+}
+
+ErrWord next_generation() { return g_generation.fetch_add(1, std::memory_order_relaxed); }
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+int tc_fault_inject() { return g_fault_inject.load(); }
+
+TcOptions resolve_tc_options(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                             int a_major, const void* B, int64_t ldb, int b_major, const void* C,
+                             int64_t ldc, int c_major, int dtype) {
+    const RunConfig c =
+        resolve(make_key(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype));
+    return TcOptions{c.cta_group, c.tc_store != 1 ? 1 : 0, c.multicast == 2 ? 1 : 0,
+                     c.tc_scheduler == 2 ? 1 : 0};
+}
+
+int check_device_pointers(const void* const* ptrs, int n, int device) {
+    for (int i = 0; i < n; ++i) {
+        if (!ptrs[i]) continue;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, ptrs[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return kInvalidArg;
+        }
+        if (at.type != cudaMemoryTypeDevice || at.device != device) return kInvalidArg;
+    }
     return kOk;
 }
 
@@ -467,6 +496,9 @@ int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_majo
         DeviceInfo* dev = nullptr;
         cudaMemPool_t pool = nullptr;
         rc = current_device(&dev, &pool);
+        if (rc != kOk) return rc;
+        const void* ptrs[3] = {K > 0 ? A : nullptr, K > 0 ? B : nullptr, C};
+        rc = check_device_pointers(ptrs, 3, dev->device);
         if (rc != kOk) return rc;
         const Problem p =
             normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
@@ -497,6 +529,9 @@ int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_m
         DeviceInfo* dev = nullptr;
         cudaMemPool_t pool = nullptr;
         rc = current_device(&dev, &pool);
+        if (rc != kOk) return rc;
+        const void* ptrs[4] = {K > 0 ? A : nullptr, K > 0 ? B : nullptr, C, epi->bias};
+        rc = check_device_pointers(ptrs, 4, dev->device);
         if (rc != kOk) return rc;
         Problem p = normalise(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype);
         // a column-major C is stored transposed: its columns are our rows
@@ -694,6 +729,9 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         cudaMemPool_t pool = nullptr;
         rc = current_device(&dev, &pool);
         if (rc != kOk) return rc;
+        const void* ptrs[3] = {A, B, C};
+        rc = check_device_pointers(ptrs, 3, dev->device);
+        if (rc != kOk) return rc;
         if (iterations <= 0) iterations = 5;
         cudaStream_t s = static_cast<cudaStream_t>(stream);
         const Problem p =
@@ -708,8 +746,10 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
                 for (int t = 1; t <= (any_kmajor ? 2 : 1); ++t) cands[n++] = {c, t, 2, 1, 0};
         } else {
             const bool c_aligned = aligned16_ld(C, ldc, out_bytes(dtype));
-            // (CTA group, multicast, scheduler); multicast runs the static one
-            const int modes[5][3] = {{1, 1, 1}, {1, 1, 2}, {2, 1, 1}, {2, 1, 2}, {2, 2, 1}};
+            // (CTA group, multicast, scheduler). The operand-multicast variant
+            // is never a candidate: it runs only when the caller asks for it
+            // (GEMM_OPT_TC_MULTICAST = 2).
+            const int modes[4][3] = {{1, 1, 1}, {1, 1, 2}, {2, 1, 1}, {2, 1, 2}};
             for (const auto& m : modes)
                 for (int st = c_aligned ? 0 : 1; st <= 1; ++st)
                     cands[n++] = {1, 0, m[0], m[1], st, 0, m[2]};
@@ -777,7 +817,10 @@ int softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float* y, in
         if (!span_ok(M, N, ldx, 4) || !span_ok(M, N, ldy, 4)) return kInvalidArg;
         if (N > softmax_max_cols()) return kUnsupported;
         DeviceInfo* dev = nullptr;
-        const int rc = current_device(&dev, nullptr);
+        int rc = current_device(&dev, nullptr);
+        if (rc != kOk) return rc;
+        const void* ptrs[2] = {x, y};
+        rc = check_device_pointers(ptrs, 2, dev->device);
         if (rc != kOk) return rc;
         return launch_softmax_rows(M, N, x, ldx, y, ldy, *dev, g_wait_limit_ns.load(),
                                    g_softmax_fault_inject.load(),
@@ -808,13 +851,13 @@ int gemm_check_device_error(void* stream) {
         cudaGetLastError();
         return kCuda;
     }
-    unsigned int word = 0;
+    ErrWord word = 0;
     if (cudaMemcpy(&word, dev->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
         cudaGetLastError();
         return kCuda;
     }
-    if (word == kDevErrNone) return kOk;
-    const unsigned int zero = 0;
+    if (word == 0) return kOk;
+    const ErrWord zero = 0;
     if (cudaMemcpy(dev->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
         cudaGetLastError();
         return kCuda;

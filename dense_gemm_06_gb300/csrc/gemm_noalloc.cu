@@ -67,7 +67,7 @@ int fixed_device(FixedDevice** out) {
             st.status = kCuda;
             return;
         }
-        unsigned int* err = nullptr;
+        ErrWord* err = nullptr;
         if (error_word_address(&err) != kOk) {
             st.status = kCuda;
             return;
@@ -85,13 +85,39 @@ int fixed_device(FixedDevice** out) {
     return kOk;
 }
 
-// Copy `outer` rows of `inner` 16-bit elements (row pitch `lds`) into the
-// fixed array at byte offset `off`, rows `ldd` elements apart.
-__global__ void repack16_fixed_kernel(const uint16_t* __restrict__ src, int64_t lds,
-                                      int64_t off, int64_t ldd, int64_t outer, int64_t inner) {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(g_fixed_scratch + off);
-    for (int64_t r = blockIdx.x; r < outer; r += gridDim.x)  // a block per row
-        for (int64_t c = threadIdx.x; c < inner; c += blockDim.x) dst[r * ldd + c] = src[r * lds + c];
+// One operand to repack into the fixed array: `outer` rows of `inner` 16-bit
+// elements, row pitch `lds` in src; in the array from byte offset `off`,
+// rows `ldd` elements apart (a multiple of 8, so each row is 16-byte aligned).
+struct FixedJob {
+    const uint16_t* src;
+    int64_t lds, off, ldd, outer, inner;
+};
+
+// Repacks up to two operands in one launch, a block per row (the rows of `a`,
+// then those of `b`): each thread gathers 8 consecutive elements of a source
+// row (any 2-byte alignment) and writes them with one 16-byte store; the last
+// inner % 8 elements of a row go one by one.
+__global__ void repack16_fixed_kernel(const FixedJob a, const FixedJob b) {
+    const int64_t rows = a.outer + b.outer;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const bool in_a = r < a.outer;
+        const FixedJob& j = in_a ? a : b;
+        const int64_t rr = in_a ? r : r - a.outer;
+        const uint16_t* __restrict__ src = j.src + rr * j.lds;
+        uint16_t* __restrict__ dst =
+            reinterpret_cast<uint16_t*>(g_fixed_scratch + j.off) + rr * j.ldd;
+        const int64_t groups = j.inner / 8;
+        for (int64_t g = threadIdx.x; g < groups; g += blockDim.x) {
+            const uint16_t* q = src + 8 * g;
+            uint4 v;
+            v.x = (uint32_t)q[0] | ((uint32_t)q[1] << 16);
+            v.y = (uint32_t)q[2] | ((uint32_t)q[3] << 16);
+            v.z = (uint32_t)q[4] | ((uint32_t)q[5] << 16);
+            v.w = (uint32_t)q[6] | ((uint32_t)q[7] << 16);
+            *reinterpret_cast<uint4*>(dst + 8 * g) = v;
+        }
+        for (int64_t c = 8 * groups + threadIdx.x; c < j.inner; c += blockDim.x) dst[c] = src[c];
+    }
 }
 
 // C = 0 for K == 0: `rows` rows of `row_bytes` bytes, `pitch` bytes apart.
@@ -120,10 +146,13 @@ extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int6
         if (M == 0 || N == 0) return kOk;
         Problem p = normalised(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major,
                                dtype);
+        FixedDevice* fd = nullptr;
+        rc = fixed_device(&fd);
+        if (rc != kOk) return rc;
+        const void* ptrs[3] = {K > 0 ? A : nullptr, K > 0 ? B : nullptr, C};
+        rc = check_device_pointers(ptrs, 3, fd->info.device);
+        if (rc != kOk) return rc;
         if (K == 0) {  // C = 0, as gemm() does
-            FixedDevice* fd = nullptr;
-            rc = fixed_device(&fd);
-            if (rc != kOk) return rc;
             const int64_t esize = dtype <= GEMM_BF16_F32 ? 4 : 2;
             int64_t blocks = p.M;  // a block per row of C
             const int64_t cap = (int64_t)fd->info.sm_count * 8;
@@ -155,30 +184,29 @@ extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int6
             used += bytes;
         }
 
-        FixedDevice* fd = nullptr;
-        rc = fixed_device(&fd);
-        if (rc != kOk) return rc;
         cudaStream_t s = static_cast<cudaStream_t>(stream);
+        FixedJob job[2] = {};  // outer == 0: nothing to repack
         for (int i = 0; i < 2; ++i) {
             if (off[i] < 0) continue;
-            int64_t blocks = outer[i];  // a block per row
-            const int64_t cap = (int64_t)fd->info.sm_count * 8;
-            if (blocks > cap) blocks = cap;
-            repack16_fixed_kernel<<<(int)(blocks < 1 ? 1 : blocks), 256, 0, s>>>(
-                static_cast<const uint16_t*>(*ops[i]), *lds[i], off[i], ld2[i], outer[i],
-                inner[i]);
-            if (cudaGetLastError() != cudaSuccess) return kCuda;
-            note_launch();
+            job[i] = {static_cast<const uint16_t*>(*ops[i]), *lds[i], off[i], ld2[i], outer[i],
+                      inner[i]};
             *ops[i] = fd->scratch + off[i];
             *lds[i] = ld2[i];
         }
-        int64_t wait = gemm_get_option(GEMM_OPT_WAIT_LIMIT_NS);
-        return launch_gemm_tc(p, fd->info, (int)gemm_get_option(GEMM_OPT_TC_CTA_GROUP),
-                              (uint64_t)(wait > 0 ? wait : 1000000000ll),
-                              (int)gemm_get_option(GEMM_OPT_TC_FAULT_INJECT),
-                              gemm_get_option(GEMM_OPT_TC_STORE) != 1,
-                              gemm_get_option(GEMM_OPT_TC_MULTICAST) == 2,
-                              gemm_get_option(GEMM_OPT_TC_SCHEDULER) == 2, s);
+        const int64_t rows_all = job[0].outer + job[1].outer;
+        if (rows_all > 0) {  // both operands in one launch, a block per row
+            const int64_t cap = (int64_t)fd->info.sm_count * 8;
+            const int64_t blocks = rows_all > cap ? cap : rows_all;
+            repack16_fixed_kernel<<<(int)blocks, 256, 0, s>>>(job[0], job[1]);
+            if (cudaGetLastError() != cudaSuccess) return kCuda;
+            note_launch();
+        }
+        // The same kernel options gemm() would resolve for this problem
+        // (caller's options, then a gemm_tune() entry, then the default).
+        const TcOptions o = resolve_tc_options(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc,
+                                               c_major, dtype);
+        return launch_gemm_tc(p, fd->info, o.cta_group, wait_limit_ns(), tc_fault_inject(),
+                              o.c_tma, o.multicast, o.clc, s);
     } catch (...) {
         return kCuda;
     }

@@ -156,6 +156,7 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     tp.c_vec = ((reinterpret_cast<uintptr_t>(pr.C) & 15u) == 0 &&
                 ((pr.ldc * out_bytes) & 15) == 0) ? 1 : 0;
     tp.err = dev.err_word;
+    tp.gen = next_generation();
     tp.wait_limit_ns = wait_limit_ns;
     tp.fault_inject = fault_inject;
     tp.clc = clc && !mc ? 1 : 0;  // the multicast variant keeps the static schedule

@@ -29,7 +29,8 @@ struct TcParams {
     int M, N, K;
     int tiles_m, tiles_n, num_kb;
     int c_vec;                 // C base / ldc allow 16-byte stores
-    unsigned int* err;         // device error word
+    ErrWord* err;              // device error word
+    ErrWord gen;               // this launch's generation (see internal.h)
     unsigned long long wait_limit_ns;
     int fault_inject;          // test hook: 1 = epilogue waits on a barrier nobody arrives at
     int clc;                   // 1: one cluster per tile, later tiles taken by try_cancel
@@ -100,17 +101,18 @@ __device__ __forceinline__ TileCoord raster(int t, int tiles_m, int tiles_n) {
     return c;
 }
 
-// Bounded wait: true when the phase completed, false on timeout / abort.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, unsigned int* err,
+// Bounded wait: true when the phase completed, false on timeout, or when
+// another wait of the same launch (generation `gen`) has already run out.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, ErrWord* err, ErrWord gen,
                                        unsigned long long limit) {
     const uint64_t t0 = globaltimer_ns();
     uint32_t n = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((++n & 31u) == 0) {
-            if (*reinterpret_cast<volatile unsigned int*>(err) != kDevErrNone) return false;
+            if (gen_failed(err, gen)) return false;
             if (globaltimer_ns() - t0 > limit) {
-                atomicCAS(err, kDevErrNone, kDevErrTimeout);
+                gen_record_timeout(err, gen);
                 return false;
             }
         }
@@ -119,7 +121,7 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, unsigned i
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const TcParams& p) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, p.err, p.wait_limit_ns);
+    return wait_slow(bar, parity, p.err, p.gen, p.wait_limit_ns);
 }
 
 // Spin (bounded by time, no barrier) to let in-flight async copies land.

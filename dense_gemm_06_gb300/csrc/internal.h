@@ -33,12 +33,34 @@ struct Problem {
     EpiParams epi;
 };
 
+// The per-device error word: 0 while no bounded wait has run out since the
+// last gemm_check_device_error(), else the largest launch generation whose
+// wait ran out. Every launch with bounded waits gets a generation of its own
+// (next_generation(), never 0); its threads give up early only when the word
+// holds that generation, so a timeout left over from an earlier launch does
+// not stop later ones.
+using ErrWord = unsigned long long;
+
 struct DeviceInfo {
     int device;
     int sm_count;
     int cc_major, cc_minor;
-    unsigned int* err_word;  // device address of this device's error word
+    ErrWord* err_word;  // device address of this device's error word
 };
+
+// A fresh launch generation (process-wide counter, starts at 1).
+ErrWord next_generation();
+
+#ifdef __CUDACC__
+// True when a wait of the launch with generation `gen` has run out.
+__device__ __forceinline__ bool gen_failed(const ErrWord* err, ErrWord gen) {
+    return *reinterpret_cast<const volatile ErrWord*>(err) == gen;
+}
+// Records that a wait of the launch `gen` ran out.
+__device__ __forceinline__ void gen_record_timeout(ErrWord* err, ErrWord gen) {
+    atomicMax(err, gen);
+}
+#endif
 
 // Launchers return 0 or a gemm_status. They enqueue exactly the kernels they
 // report through note_launch().
@@ -94,7 +116,27 @@ int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int 
 Problem normalised(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,
                    const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
                    int dtype);
-int error_word_address(unsigned int** out);
+int error_word_address(ErrWord** out);
+// kOk when every non-null pointer of ptrs[0..n) is device memory of device
+// `device` (cudaPointerGetAttributes: type device, same ordinal), else
+// kInvalidArg. Host, managed and peer-device pointers are rejected before any
+// launch, so no kernel -- in particular no cluster-multicast TMA load -- ever
+// addresses another GPU's memory.
+int check_device_pointers(const void* const* ptrs, int n, int device);
+// The tensor-core kernel options gemm() resolves for a problem: an option the
+// caller set wins, then a gemm_tune() entry for the problem, then the default.
+struct TcOptions {
+    int cta_group;  // 1 or 2
+    int c_tma;      // 1: TMA stores where C allows, 0: st.global only
+    int multicast;  // 1: B multicast across two pairs (only when the option asks)
+    int clc;        // 1: cluster-launch-control scheduler
+};
+TcOptions resolve_tc_options(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                             int a_major, const void* B, int64_t ldb, int b_major, const void* C,
+                             int64_t ldc, int c_major, int dtype);
+// The GEMM_OPT_WAIT_LIMIT_NS and GEMM_OPT_TC_FAULT_INJECT values.
+uint64_t wait_limit_ns();
+int tc_fault_inject();
 
 // Row softmax over thread-block clusters (softmax_cluster.cu); rows longer
 // than softmax_max_cols() are not supported.
@@ -116,10 +158,5 @@ enum : int {
     kTimeout = -4,
 };
 
-// Codes kernels write into the device error word.
-enum : unsigned int {
-    kDevErrNone = 0,
-    kDevErrTimeout = 1,
-};
 
 }  // namespace libgemm

@@ -41,7 +41,8 @@ int launch_tma(SgemmParams sp, const CUtensorMap& ta, const CUtensorMap& tb,
             sp.splits = 1;
         }
     }
-    const TmaArgs x{dev.err_word, (unsigned long long)wait_limit_ns, fault_inject};
+    const TmaArgs x{dev.err_word, next_generation(), (unsigned long long)wait_limit_ns,
+                    fault_inject};
     const int64_t units =
         sp.dp_tiles + ((int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles) * sp.splits;
     kern<<<dim3((unsigned)units), dim3(Cfg::THREADS), TC::SMEM, stream>>>(sp, ta, tb, x);

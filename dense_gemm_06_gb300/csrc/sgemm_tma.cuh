@@ -48,23 +48,24 @@ struct TmaCfg {
 };
 
 struct TmaArgs {
-    unsigned int* err;         // device error word
+    ErrWord* err;              // device error word
+    ErrWord gen;               // this launch's generation (see internal.h)
     unsigned long long limit;  // wait limit, ns
     int fault;                 // test hook: CTA 0 never loads its k-tile 1
 };
 
 // Bounded wait on a phase: true when it completed, false on timeout (or when
-// another wait has already failed).
-__device__ __noinline__ bool sg_wait_slow(uint32_t bar, uint32_t parity, unsigned int* err,
-                                          unsigned long long limit) {
+// another wait of the same launch, generation `gen`, has already failed).
+__device__ __noinline__ bool sg_wait_slow(uint32_t bar, uint32_t parity, ErrWord* err,
+                                          ErrWord gen, unsigned long long limit) {
     const uint64_t t0 = globaltimer_ns();
     uint32_t n = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((++n & 31u) == 0) {
-            if (*reinterpret_cast<volatile unsigned int*>(err) != kDevErrNone) return false;
+            if (gen_failed(err, gen)) return false;
             if (globaltimer_ns() - t0 > limit) {
-                atomicCAS(err, kDevErrNone, kDevErrTimeout);
+                gen_record_timeout(err, gen);
                 return false;
             }
         }
@@ -73,7 +74,7 @@ __device__ __noinline__ bool sg_wait_slow(uint32_t bar, uint32_t parity, unsigne
 
 __device__ __forceinline__ bool sg_wait(uint32_t bar, uint32_t parity, const TmaArgs& x) {
     if (mbar_try_wait(bar, parity)) return true;
-    return sg_wait_slow(bar, parity, x.err, x.limit);
+    return sg_wait_slow(bar, parity, x.err, x.gen, x.limit);
 }
 
 // After a failed wait: thread 0 waits (bounded, ignoring the error word) for

@@ -44,7 +44,8 @@ struct SoftmaxParams {
     int M, N;
     int cta_cols;  // columns per CTA (a multiple of 4)
     int cs;        // CTAs per row (cluster size)
-    unsigned int* err;             // device error word (bounded waits)
+    ErrWord* err;                  // device error word (bounded waits)
+    ErrWord gen;                   // this launch's generation (see internal.h)
     unsigned long long wait_limit_ns;
     int fault_inject;              // test hook: row 0's first CTA withholds its partial
 };
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(THREADS) softmax_cluster_push_kernel(const Sof
             while (!(done = mbar_try_wait(xb, 0u))) {
                 if ((++n & 31u) == 0) {
                     if (t0 == 0) t0 = globaltimer_ns();
-                    if (*reinterpret_cast<volatile unsigned int*>(p.err) != kDevErrNone ||
+                    if (gen_failed(p.err, p.gen) ||
                         globaltimer_ns() - t0 > p.wait_limit_ns)
                         break;
                 }
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(THREADS) softmax_cluster_push_kernel(const Sof
         if (lane == 0) {
             row_m_s = m;
             row_s_s = s;
-            if (!ok) atomicCAS(p.err, kDevErrNone, kDevErrTimeout);
+            if (!ok) gen_record_timeout(p.err, p.gen);
         }
     }
     __syncthreads();
@@ -458,8 +459,8 @@ int launch_softmax_rows(int64_t M, int64_t N, const float* x, int64_t ldx, float
     const bool vec = (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(y) & 15u) == 0 && (ldx & 3) == 0 &&
                      (ldy & 3) == 0;
-    SoftmaxParams sp{x, y, ldx, ldy, (int)M, (int)N, 0, 1, dev.err_word, wait_limit_ns,
-                     fault_inject};
+    SoftmaxParams sp{x, y, ldx, ldy, (int)M, (int)N, 0, 1, dev.err_word, next_generation(),
+                     wait_limit_ns, fault_inject};
     if (vec && N >= PUSH_MIN_N && N <= (int64_t)MAX_CLUSTER * PUSH_COLS)
         return launch_push_rows(sp, dev.device, stream);
     if (N <= WARP_ROWS_MAX_N) {

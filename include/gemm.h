@@ -44,7 +44,12 @@
  * nothing); K == 0 writes C = 0. Negative sizes are GEMM_ERR_INVALID_ARG.
  *
  * Execution and ownership: the caller owns A, B and C. gemm() takes DEVICE
- * pointers of the current device, is asynchronous on `stream` (a
+ * pointers of the current device -- memory from cudaMalloc, cudaMallocAsync
+ * or a device memory pool of that device (cudaPointerGetAttributes reports
+ * type device and the current ordinal). Host memory (pinned or pageable),
+ * managed memory and other GPUs' memory are GEMM_ERR_INVALID_ARG, checked
+ * before any launch: the library runs on one GPU and no kernel of it ever
+ * addresses another GPU's memory. gemm() is asynchronous on `stream` (a
  * cudaStream_t of the current device; NULL = legacy default stream) and never
  * synchronises. C overlapping A or B is undefined
  * and not checked. Scratch for repacking misaligned operands comes from a
@@ -54,8 +59,9 @@
  *
  * Errors: every entry point returns GEMM_OK (0) or a negative status:
  *     GEMM_ERR_INVALID_ARG  bad size, pointer, leading dimension, enum or
- *                           alignment; checked on the host before any CUDA
- *                           call, nothing is launched
+ *                           alignment, or an operand that is not device
+ *                           memory of the current device; checked on the
+ *                           host before any launch
  *     GEMM_ERR_UNSUPPORTED  no usable device, or the device is not sm_103
  *     GEMM_ERR_CUDA         a CUDA runtime call failed (allocation, copy,
  *                           tensor-map encode, launch)
@@ -63,11 +69,12 @@
  *                           waiting on a pipeline barrier after its time
  *                           limit and wrote no trustworthy C
  * Device-side timeouts are reported asynchronously: a kernel that times out
- * records it in a per-device error word and returns; gemm_check_device_error
- * reads and clears that word. While the word is set, tensor-core kernels on
- * that device stop at their first wait that does not complete at once, so
- * results computed between a timeout and the next gemm_check_device_error
- * are not to be trusted.
+ * records it in a per-device error word and returns without a trustworthy C;
+ * gemm_check_device_error reads and clears that word. Every launch carries a
+ * generation number of its own and gives up early only on a timeout of its
+ * own generation, so a timeout does not spill over into later launches: a
+ * GEMM launched after another one timed out, before anyone called
+ * gemm_check_device_error, still runs to completion and is correct.
  */
 #ifndef LIBGEMM_GEMM_H
 #define LIBGEMM_GEMM_H
@@ -185,8 +192,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K,
  * different threads without ordering -- race on the array; order them on one
  * stream. The first call on a device looks the array up on that device
  * (cudaGetSymbolAddress) and caches the address; make that first call before
- * any stream capture. Otherwise arguments, layouts, status codes and
- * asynchrony are those of gemm().
+ * any stream capture. It runs the kernel configuration gemm() would run for
+ * the same problem (options, then a gemm_tune entry, then the default).
+ * Otherwise arguments, layouts, status codes and asynchrony are those of
+ * gemm().
  */
 int gemm_noalloc(int64_t M, int64_t N, int64_t K,
                  const void *A, int64_t lda, int a_major,
@@ -212,7 +221,8 @@ typedef struct gemm_tuning {
  * gemm_tune -- per-problem configuration selection (the pages' autotune
  * utilities, CuTe DSL `tune`/`autotune_jit`, done natively): runs every
  * kernel configuration valid for this problem on the caller's buffers and
- * stream (one warm-up call and `iterations` timed calls each, CUDA events),
+ * stream (one warm-up call and `iterations` timed calls each, CUDA events;
+ * the operand-multicast variant is never a candidate),
  * records the fastest in a process-wide table keyed by (M, N, K, dtype,
  * majors, 16-byte alignment of A, B and C) and writes it to *out (may be
  * NULL). Later gemm(), gemm_ex() and gemm_host() calls on a matching problem
@@ -319,9 +329,11 @@ enum gemm_option {
        chunks), 1 = always st.global. */
     GEMM_OPT_TC_STORE = 6,
     /* Operand multicast in the 2-CTA tensor-core kernel: 0 = automatic
-       (currently off), 1 = off, 2 = on: clusters of two CTA pairs compute
-       vertically adjacent 256 x 256 tiles and each half of the shared B tile
-       is loaded once per cluster and multicast by TMA to both pairs. */
+       (off; gemm_tune never selects it), 1 = off, 2 = on: clusters of two CTA
+       pairs compute vertically adjacent 256 x 256 tiles and each half of the
+       shared B tile is loaded once per cluster and multicast by TMA to both
+       pairs. The multicast copies only ever address memory of the current
+       device: every operand is checked to be this GPU's memory first. */
     GEMM_OPT_TC_MULTICAST = 7,
     /* Test hook for softmax_rows' timeout path: 1 makes the first CTA of the
        first row's cluster (aligned rows of 16385..262144 columns) withhold

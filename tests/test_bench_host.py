@@ -1,13 +1,10 @@
-"""Host-side logic of bench.py on the CPU: the replica path's barrier and
-max-over-ranks timing on a world-size-2 gloo group, the whole-job
-throughput, the reference arm's rank handling and the clock-record summary."""
+"""Host-side logic of bench.py on the CPU: the throughput arithmetic, the
+single-GPU argument rule, the clock-record summary, the peaks and the
+source-keyed traffic record."""
 
-import io
 import json
 import os
-import socket
 import sys
-from contextlib import redirect_stdout
 
 import pytest
 
@@ -16,62 +13,26 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
-
-
-def _worker(rank, world, port, q):
-    import torch
-    import torch.distributed as dist
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    try:
-        bench.barrier(world)
-        slow = bench.max_over_ranks(10.0 + 5.0 * rank, world, torch.device("cpu"))
-        bench.barrier(world)
-        q.put((rank, slow))
-    finally:
-        dist.destroy_process_group()
-
-
-def test_two_rank_barrier_and_max_time():
-    import torch.multiprocessing as mp
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(timeout=120)
-        assert p.exitcode == 0
-    got = sorted(q.get(timeout=10) for _ in range(2))
-    assert got == [(0, 15.0), (1, 15.0)]   # every rank sees the slowest rank's time
-
-
-def test_single_rank_needs_no_group():
-    assert bench.max_over_ranks(3.5, 1, None) == 3.5
-    bench.barrier(1)
-
-
-def test_throughput_is_weak_scaling_over_replicas():
+def test_throughput():
     f = 5 * 2.0 * 8192 ** 3
-    one = bench.throughput_tflops(f, 10, 1, 680.0)
-    two = bench.throughput_tflops(f, 10, 2, 680.0)
-    assert two == pytest.approx(2 * one)
+    one = bench.throughput_tflops(f, 10, 680.0)
     assert one == pytest.approx(f * 10 / 0.68 / 1e12)
+    assert bench.throughput_tflops(f, 20, 680.0) == pytest.approx(2 * one)
 
 
-def test_reference_arm_rank_nonzero_exits_quietly(monkeypatch):
-    monkeypatch.setenv("RANK", "1")
-    monkeypatch.setenv("WORLD_SIZE", "2")
-    buf = io.StringIO()
-    with redirect_stdout(buf):
-        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"])
-    assert buf.getvalue() == ""
+@pytest.mark.parametrize("impl", ["native", "reference"])
+def test_only_one_gpu_is_accepted(impl):
+    # the library is single-GPU: any other --gpus is refused before anything runs
+    for n in (0, 2, 8):
+        with pytest.raises(SystemExit) as e:
+            bench.main(["--impl", impl, "--gpus", str(n), "--steps", "1", "--warmup", "0"])
+        assert e.value.code == 2
+
+
+def test_no_process_group_code_left():
+    # no torch.distributed / NCCL path remains in the benchmark
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert "torch.distributed" not in src and "init_process_group" not in src
 
 
 def test_clock_summary():

@@ -115,3 +115,58 @@ def test_withheld_softmax_partial_times_out_and_device_recovers():
     y = dy.cpu().numpy().astype(np.float64)
     y_ref = oracle.softmax_ref(M, N, x.ravel(), N)
     assert np.all(np.abs(y - y_ref) <= 1e-5 * y_ref + 1e-30)
+
+
+def _gemm_without_check(M, N, K, dtype, A, lda, am, B, ldb, bm):
+    """gemm() through the C ABI, C read back WITHOUT gemm_check_device_error."""
+    import torch
+    from gpu_util import CBuffer, to_device
+    cbuf = CBuffer(M, N, 1, N, lg.OUT_TYPE[dtype])
+    lg.check(lg.gemm(M, N, K, to_device(A), lda, am, to_device(B), ldb, bm, cbuf.ptr(), N, 1,
+                     dtype), "gemm")
+    torch.cuda.synchronize()
+    return cbuf.read()
+
+
+@pytest.mark.parametrize("kernel", ["tcgen05", "ffma_tma"])
+def test_timeout_is_confined_to_its_launch(kernel):
+    # A wait of one launch runs out; the next launch -- made while the error
+    # word still records that timeout (nobody has called
+    # gemm_check_device_error) -- must run to the end and be exact, and the
+    # check afterwards reports exactly one timeout.
+    import torch
+    hook = lg.GEMM_OPT_TC_FAULT_INJECT if kernel == "tcgen05" else lg.GEMM_OPT_SIMT_FAULT_INJECT
+    saved = {o: lg.gemm_get_option(o) for o in (lg.GEMM_OPT_WAIT_LIMIT_NS, hook,
+                                                lg.GEMM_OPT_SIMT_CONFIG)}
+    assert lg.gemm_check_device_error() == lg.GEMM_OK
+    try:
+        lg.check(lg.gemm_set_option(lg.GEMM_OPT_WAIT_LIMIT_NS, 20_000_000))
+        if kernel == "tcgen05":
+            n, k = 4096, 512
+            dA = torch.zeros(n * k, dtype=torch.int16, device="cuda")
+            dB = torch.zeros(n * k, dtype=torch.int16, device="cuda")
+            dC = torch.zeros(n * n, dtype=torch.int16, device="cuda")
+            lg.check(lg.gemm_set_option(hook, 1))
+            assert lg.gemm(n, n, k, dA, k, 0, dB, k, 0, dC, n, 1, lg.GEMM_BF16_BF16) == lg.GEMM_OK
+            dtype = lg.GEMM_F16_F32
+        else:
+            M, N, K = 512, 512, 256
+            dA = torch.zeros(K * M, dtype=torch.float32, device="cuda")
+            dB = torch.zeros(K * N, dtype=torch.float32, device="cuda")
+            dC = torch.zeros(M * N, dtype=torch.float32, device="cuda")
+            lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_CONFIG, 9))
+            lg.check(lg.gemm_set_option(hook, 1))
+            assert lg.gemm(M, N, K, dA, M, 1, dB, N, 1, dC, N, 1, lg.GEMM_F32) == lg.GEMM_OK
+            dtype = lg.GEMM_F32
+        torch.cuda.synchronize()  # the first launch has timed out and exited
+        lg.check(lg.gemm_set_option(hook, 0))
+        am = 0 if kernel == "tcgen05" else 1
+        A, lda, B, ldb = make_operands(600, 520, 300, dtype, am, 1, "int", 5)
+        C = _gemm_without_check(600, 520, 300, dtype, A, lda, am, B, ldb, 1)
+        check_full(C, 600, 520, 300, dtype, A, lda, am, B, ldb, 1, exact=True,
+                   what=f"{kernel} launch after another launch's timeout")
+        assert lg.gemm_check_device_error() == lg.GEMM_ERR_TIMEOUT  # the first launch's
+        assert lg.gemm_check_device_error() == lg.GEMM_OK
+    finally:
+        for o, v in saved.items():
+            lg.gemm_set_option(o, v)
