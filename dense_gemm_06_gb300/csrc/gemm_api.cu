@@ -21,6 +21,7 @@
 #include "epilogue.cuh"
 #include "internal.h"
 #include "policy.h"
+#include "repack16.cuh"
 
 namespace libgemm {
 
@@ -209,41 +210,6 @@ __global__ void zero_rows_kernel(uint8_t* C, int64_t rows, int64_t row_bytes,
         for (int64_t c = threadIdx.x; c < row_bytes; c += blockDim.x) C[r * pitch_bytes + c] = 0;
 }
 
-// One 16-bit operand to repack: `outer` rows of `inner` elements, row pitch
-// `lds` in src and `ldd` in dst (a multiple of 8 elements, so dst rows are
-// 16-byte aligned for TMA).
-struct Repack16 {
-    const uint16_t* src;
-    uint16_t* dst;
-    int64_t lds, ldd, outer, inner;
-};
-
-// Repacks up to two operands in one launch: a block per row (the rows of `a`,
-// then those of `b`); each thread gathers 8 consecutive elements of a row
-// (the source rows have any 2-byte alignment) and writes them with one
-// 16-byte store, the last inner % 8 elements one by one.
-__global__ void repack16_kernel(const Repack16 a, const Repack16 b) {
-    const int64_t rows = a.outer + b.outer;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const bool in_a = r < a.outer;
-        const int64_t rr = in_a ? r : r - a.outer;
-        const int64_t inner = in_a ? a.inner : b.inner;
-        const uint16_t* __restrict__ src = (in_a ? a.src : b.src) + rr * (in_a ? a.lds : b.lds);
-        uint16_t* __restrict__ dst = (in_a ? a.dst : b.dst) + rr * (in_a ? a.ldd : b.ldd);
-        const int64_t groups = inner / 8;
-        for (int64_t g = threadIdx.x; g < groups; g += blockDim.x) {
-            const uint16_t* q = src + 8 * g;
-            uint4 v;
-            v.x = (uint32_t)q[0] | ((uint32_t)q[1] << 16);
-            v.y = (uint32_t)q[2] | ((uint32_t)q[3] << 16);
-            v.z = (uint32_t)q[4] | ((uint32_t)q[5] << 16);
-            v.w = (uint32_t)q[6] | ((uint32_t)q[7] << 16);
-            *reinterpret_cast<uint4*>(dst + 8 * g) = v;
-        }
-        for (int64_t c = 8 * groups + threadIdx.x; c < inner; c += blockDim.x) dst[c] = src[c];
-    }
-}
-
 // Blocks for a row-per-block kernel over `rows` rows: at most 8 per SM.
 int grid_rows(int64_t rows, const DeviceInfo& dev) {
     const int64_t cap = (int64_t)dev.sm_count * 8;
@@ -347,8 +313,8 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCo
         *lds[i] = ld2;
     }
     if (rc == kOk && job[0].outer + job[1].outer > 0) {  // both operands in one launch
-        repack16_kernel<<<grid_rows(job[0].outer + job[1].outer, dev), 256, 0, s>>>(job[0],
-                                                                                   job[1]);
+        repack16_kernel<<<repack16_blocks(job[0].outer + job[1].outer, dev.sm_count), 256, 0,
+                          s>>>(job[0], job[1]);
         if (cudaGetLastError() != cudaSuccess) rc = kCuda;
         else note_launch();
     }

@@ -23,6 +23,7 @@
 
 #include "../../include/gemm.h"
 #include "internal.h"
+#include "repack16.cuh"
 
 namespace libgemm {
 namespace {
@@ -83,41 +84,6 @@ int fixed_device(FixedDevice** out) {
     if (st.status != kOk) return st.status;
     *out = &st;
     return kOk;
-}
-
-// One operand to repack into the fixed array: `outer` rows of `inner` 16-bit
-// elements, row pitch `lds` in src; in the array from byte offset `off`,
-// rows `ldd` elements apart (a multiple of 8, so each row is 16-byte aligned).
-struct FixedJob {
-    const uint16_t* src;
-    int64_t lds, off, ldd, outer, inner;
-};
-
-// Repacks up to two operands in one launch, a block per row (the rows of `a`,
-// then those of `b`): each thread gathers 8 consecutive elements of a source
-// row (any 2-byte alignment) and writes them with one 16-byte store; the last
-// inner % 8 elements of a row go one by one.
-__global__ void repack16_fixed_kernel(const FixedJob a, const FixedJob b) {
-    const int64_t rows = a.outer + b.outer;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const bool in_a = r < a.outer;
-        const FixedJob& j = in_a ? a : b;
-        const int64_t rr = in_a ? r : r - a.outer;
-        const uint16_t* __restrict__ src = j.src + rr * j.lds;
-        uint16_t* __restrict__ dst =
-            reinterpret_cast<uint16_t*>(g_fixed_scratch + j.off) + rr * j.ldd;
-        const int64_t groups = j.inner / 8;
-        for (int64_t g = threadIdx.x; g < groups; g += blockDim.x) {
-            const uint16_t* q = src + 8 * g;
-            uint4 v;
-            v.x = (uint32_t)q[0] | ((uint32_t)q[1] << 16);
-            v.y = (uint32_t)q[2] | ((uint32_t)q[3] << 16);
-            v.z = (uint32_t)q[4] | ((uint32_t)q[5] << 16);
-            v.w = (uint32_t)q[6] | ((uint32_t)q[7] << 16);
-            *reinterpret_cast<uint4*>(dst + 8 * g) = v;
-        }
-        for (int64_t c = 8 * groups + threadIdx.x; c < j.inner; c += blockDim.x) dst[c] = src[c];
-    }
 }
 
 // C = 0 for K == 0: `rows` rows of `row_bytes` bytes, `pitch` bytes apart.
@@ -185,19 +151,19 @@ extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int6
         }
 
         cudaStream_t s = static_cast<cudaStream_t>(stream);
-        FixedJob job[2] = {};  // outer == 0: nothing to repack
+        Repack16 job[2] = {};  // outer == 0: nothing to repack
         for (int i = 0; i < 2; ++i) {
             if (off[i] < 0) continue;
-            job[i] = {static_cast<const uint16_t*>(*ops[i]), *lds[i], off[i], ld2[i], outer[i],
+            uint16_t* dst = reinterpret_cast<uint16_t*>(fd->scratch + off[i]);
+            job[i] = {static_cast<const uint16_t*>(*ops[i]), dst, *lds[i], ld2[i], outer[i],
                       inner[i]};
-            *ops[i] = fd->scratch + off[i];
+            *ops[i] = dst;
             *lds[i] = ld2[i];
         }
         const int64_t rows_all = job[0].outer + job[1].outer;
-        if (rows_all > 0) {  // both operands in one launch, a block per row
-            const int64_t cap = (int64_t)fd->info.sm_count * 8;
-            const int64_t blocks = rows_all > cap ? cap : rows_all;
-            repack16_fixed_kernel<<<(int)blocks, 256, 0, s>>>(job[0], job[1]);
+        if (rows_all > 0) {  // both operands in one launch, a warp per row
+            repack16_kernel<<<repack16_blocks(rows_all, fd->info.sm_count), 256, 0, s>>>(job[0],
+                                                                                       job[1]);
             if (cudaGetLastError() != cudaSuccess) return kCuda;
             note_launch();
         }

@@ -55,6 +55,9 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
+#ifdef LIBGEMM_TC_TRACE
+unsigned long long* g_trace = nullptr;  // debug build: the phase-timestamp buffer
+#endif
 
 bool get_encoder() {
     std::call_once(g_encode_once, [] {
@@ -160,6 +163,9 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     tp.wait_limit_ns = wait_limit_ns;
     tp.fault_inject = fault_inject;
     tp.clc = clc && !mc ? 1 : 0;  // the multicast variant keeps the static schedule
+#ifdef LIBGEMM_TC_TRACE
+    tp.trace = g_trace;
+#endif
     if ((int64_t)tp.tiles_m * tp.tiles_n * CG > 0x7fffffffLL) return kUnsupported;
 
     const bool a_mn = !pr.a_kmajor, b_mn = !pr.b_kmajor;
@@ -173,3 +179,11 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
 }
 
 }  // namespace libgemm
+
+#ifdef LIBGEMM_TC_TRACE
+// Debug build only: device buffer of 64 timestamps per CTA for the next
+// launches of the tensor-core kernel (NULL: no tracing).
+extern "C" void libgemm_tc_trace_buffer(void* dev_ptr) {
+    libgemm::g_trace = static_cast<unsigned long long*>(dev_ptr);
+}
+#endif

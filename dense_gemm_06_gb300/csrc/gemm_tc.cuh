@@ -35,7 +35,25 @@ struct TcParams {
     int fault_inject;          // test hook: 1 = epilogue waits on a barrier nobody arrives at
     int clc;                   // 1: one cluster per tile, later tiles taken by try_cancel
     EpiParams epi;             // fused epilogue (inactive for a plain GEMM)
+#ifdef LIBGEMM_TC_TRACE
+    unsigned long long* trace;  // debug build: per-CTA phase timestamps (64 per CTA)
+#endif
 };
+
+// Phase timestamps of the debug build (-DLIBGEMM_TC_TRACE): %globaltimer at
+// fixed points of every role, 64 slots per CTA, for reading the kernel's
+// timeline on the host. Compiled out of the library.
+#ifdef LIBGEMM_TC_TRACE
+#define TC_TRACE(p, slot)                                                              \
+    do {                                                                               \
+        if ((p).trace && (slot) < 64)                                                  \
+            (p).trace[(size_t)blockIdx.x * 64 + (slot)] = gemm_ptx::globaltimer_ns();  \
+    } while (0)
+#else
+#define TC_TRACE(p, slot) \
+    do {                  \
+    } while (0)
+#endif
 
 // Launches the kernel variant for CTA group cg (1 or 2), operand multicast mc
 // and the operand majors; defined in gemm_tc_<in>_<out>.cu.
@@ -59,8 +77,9 @@ constexpr int TILE_N = 256;      // N per tile (per CTA pair when CG == 2)
 constexpr int ROWS_A = 128;      // A rows per CTA (= TMEM lanes)
 constexpr int ACC_COLS = 256;    // TMEM columns per accumulator
 constexpr int TMEM_COLS = 512;   // two accumulators
-constexpr int THREADS = 256;
-constexpr int EPI_WARP0 = 4;     // epilogue warps 4..7 (warp % 4 == TMEM lane quarter)
+constexpr int EPI_WARP0 = 4;     // epilogue warps 4..11 (warp % 4 == TMEM lane quarter)
+constexpr int EPI_WARPS = 8;     // two per TMEM lane quarter, each storing half the chunks
+constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int BAND = 8;          // tile rows per raster band
 constexpr int CLC_SLOTS = 3;     // cluster-launch-control responses in flight
 
@@ -79,8 +98,9 @@ template <int CG> struct Cfg {
     static constexpr int RESP_OFFSET = (NUM_BARS * 8 + 8 + 15) / 16 * 16;
     static constexpr int BAR_BYTES = RESP_OFFSET + 16 * CLC_SLOTS;
     // epilogue staging: one 32 x 128-byte tile per epilogue warp
-    static constexpr int EPI_BYTES = 4 * 32 * 128;
+    static constexpr int EPI_BYTES = EPI_WARPS * 32 * 128;
     static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + align slack
+    static_assert(SMEM_BYTES <= 232448, "over the 227 KB of shared memory a CTA may use");
 };
 
 
@@ -287,45 +307,50 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
     constexpr int PER_UNIT = 16 / ES;           // elements per 16-byte unit
     constexpr int UNITS = 32 / PER_UNIT;        // 16-byte units per row
     constexpr int ROWS_PER_PASS = 32 / UNITS;
+    // Rows of this chunk inside C, and the chunk's first row in C (as bytes).
+    const int rows = min(32, p.M - row0);
+    const int64_t step = p.ldc * ES;
     if (p.c_vec && col0 + 32 <= p.N) {
         const int u = lane % UNITS;
+        char* dst = reinterpret_cast<char*>(p.C) +
+                    ((int64_t)(row0 + lane / UNITS) * p.ldc + col0 + u * PER_UNIT) * ES;
 #pragma unroll
         for (int j = 0; j < 32 / ROWS_PER_PASS; ++j) {
             const int r = j * ROWS_PER_PASS + lane / UNITS;
             const uint4 val =
                 lds128(stage + (uint32_t)(r * ROW_BYTES) + (uint32_t)((u ^ swz<ES>(r)) * 16));
-            if (row0 + r < p.M) {
-                OutT* dst = static_cast<OutT*>(p.C) + (int64_t)(row0 + r) * p.ldc + col0 + u * PER_UNIT;
-                *reinterpret_cast<uint4*>(dst) = val;
-            }
+            if (r < rows) *reinterpret_cast<uint4*>(dst) = val;
+            dst += ROWS_PER_PASS * step;
         }
     } else {
-        // Lane = column; one coalesced row segment per store. The shared
-        // loads of RB rows are issued together before their stores, so their
-        // latencies overlap instead of adding up row by row.
-        constexpr int RB = 8;
+        // Lane = column; one coalesced row segment per store. Everything that
+        // does not change from row to row is computed once: the lane's shared
+        // offset for each of the 8 swizzle phases, the row pointer (advanced
+        // by the row pitch) and the row bound. The shared loads of 8 rows are
+        // issued together before their stores, so their latencies overlap.
         const int col = col0 + lane;
         const bool col_ok = col < p.N;
         const int u = lane / PER_UNIT, e = lane % PER_UNIT;
-#pragma unroll 1
-        for (int rb = 0; rb < 32; rb += RB) {
-            uint32_t val[RB];
+        uint32_t xs[8];
 #pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                const int r = rb + i;
-                const uint32_t a = stage + (uint32_t)(r * ROW_BYTES) +
-                                   (uint32_t)((u ^ swz<ES>(r)) * 16) + (uint32_t)(e * ES);
+        for (int k = 0; k < 8; ++k) xs[k] = stage + (uint32_t)(((u ^ k) * 16) + e * ES);
+        char* dst = reinterpret_cast<char*>(p.C) + ((int64_t)row0 * p.ldc + col) * ES;
+#pragma unroll
+        for (int rb = 0; rb < 32; rb += 8) {
+            uint32_t val[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t a = xs[swz<ES>(rb + i)] + (uint32_t)((rb + i) * ROW_BYTES);
                 if constexpr (ES == 4) val[i] = lds32(a);
                 else val[i] = lds16(a);
             }
 #pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                const int r = rb + i;
-                if (row0 + r < p.M && col_ok) {
-                    OutT* dst = static_cast<OutT*>(p.C) + (int64_t)(row0 + r) * p.ldc + col;
+            for (int i = 0; i < 8; ++i) {
+                if (rb + i < rows && col_ok) {
                     if constexpr (ES == 4) *reinterpret_cast<uint32_t*>(dst) = val[i];
                     else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)val[i];
                 }
+                dst += step;
             }
         }
     }
@@ -363,6 +388,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) TC_TRACE(p, 0);
     const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;  // rank in the cluster
     const uint32_t rank = crank & (uint32_t)(CG - 1);          // rank in the CTA pair
     const int pair = MC ? (int)(crank >> 1) : 0;               // pair in the cluster
@@ -413,14 +439,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), CG * 4);  // every epilogue warp of the pair
+            mbar_init(acce_bar(a), CG * EPI_WARPS);  // every epilogue warp of the pair
         }
         mbar_init(drain_bar, 1);
         mbar_init(never_bar, 1);
         for (int s = 0; s < CLC_SLOTS; ++s) {
             mbar_init(ready_bar(s), 1);  // this CTA's scheduler thread arms it
             // consumers of the pair: producers, the MMA thread, epilogue warps
-            mbar_init(cons_bar(s), CG == 2 ? 11 : 6);
+            mbar_init(cons_bar(s), CG * (1 + EPI_WARPS) + 1);
         }
         fence_mbarrier_init_cluster();
     }
@@ -432,6 +458,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    if (threadIdx.x == 0) TC_TRACE(p, 1);
 
     bool aborted = false;
 
@@ -453,6 +480,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                     const uint32_t sa = sA0 + stage * C_::A_BYTES;
                     const uint32_t sb = sB0 + stage * C_::B_BYTES;
                     const int k0 = kb * BK;
+                    if (kb == 0 && t == cluster) TC_TRACE(p, 2);
                     if constexpr (!A_MN) {
                         tma_load_2d<CG>(sa, &p.tmap_a, fb, k0, a_row);
                     } else {
@@ -492,13 +520,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             int acc = 0;
             uint32_t acc_phase = 0;
             int j = 0;
+            int nt = 0;  // tiles issued (trace slots)
             for (int t = cluster; t < total_tiles && !aborted;) {
                 if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, p)) { aborted = true; break; }
                 tc_fence_after_sync();
+                TC_TRACE(p, 4 + 4 * nt);
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(full_bar(stage), phase, p)) { aborted = true; break; }
                     tc_fence_after_sync();
+                    if (kb == 0 && nt == 0) TC_TRACE(p, 3);
                     const uint32_t sa = sA0 + stage * C_::A_BYTES;
                     const uint32_t sb = sB0 + stage * C_::B_BYTES;
 #pragma unroll
@@ -520,6 +551,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 if (aborted) break;
                 if constexpr (MC) mma_commit_pair(accf_bar(acc), (uint16_t)(0x3u << (2 * pair)));
                 else mma_commit<CG>(accf_bar(acc));
+                TC_TRACE(p, 5 + 4 * nt);
+                ++nt;
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
                 if (!advance(t, j, false)) { aborted = true; break; }
             }
@@ -533,7 +566,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         __syncwarp();
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------ epilogue --
-        const int q = warp - EPI_WARP0;  // TMEM lane quarter of this warp
+        // TMEM lane quarter of this warp (hardware: warp % 4) and its half of
+        // the 32-column chunks (even or odd)
+        const int q = (warp - EPI_WARP0) & 3;
+        const int half = (warp - EPI_WARP0) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
         // Every lane waits; the decision to go on is taken warp-uniformly
@@ -543,6 +579,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             if (!__all_sync(0xffffffffu, wait_bar(never_bar, 0u, p))) aborted = true;
         }
         int j = 0;
+        int nt = 0;  // tiles stored (trace slots)
         for (int t = cluster; t < total_tiles && !aborted;) {
             const TileCoord tc = tile_of(t);
             if (!__all_sync(0xffffffffu, wait_bar(accf_bar(acc), acc_phase, p))) {
@@ -550,15 +587,19 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 break;
             }
             tc_fence_after_sync();
+            if (warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 6 + 4 * nt);
             const int row0 = tc.tm * C_::TILE_M + (int)rank * ROWS_A + q * 32;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            const uint32_t stage = epi0 + (uint32_t)(q * 32 * 128);
+            const uint32_t stage = epi0 + (uint32_t)((warp - EPI_WARP0) * 32 * 128);
 #pragma unroll 1
-            for (int c = 0; c < ACC_COLS / 32; ++c) {
+            for (int c = half; c < ACC_COLS / 32; c += 2) {
                 uint32_t v[32];
+                if (nt == 0 && warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 20 + 4 * c);
                 tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
                 tmem_wait_ld();
+                if (nt == 0 && warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 21 + 4 * c);
                 store_chunk<OutT>(p, stage, lane, row0, tc.tn * TILE_N + c * 32, v);
+                if (nt == 0 && warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 22 + 4 * c);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -566,11 +607,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(acce_bar(acc), lead));
                 else mbar_arrive_local(acce_bar(acc));
             }
+            if (warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 7 + 4 * nt);
+            ++nt;
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             if (!advance(t, j, true)) { aborted = true; break; }
         }
         if (p.c_tma && lane == 0) bulk_wait_all();  // stores done before the CTA exits
         __syncwarp();
+        if (warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 62);
     } else if (warp == 2) {
         // --------------------------------------- tile scheduler (CLC) --
         // Each CTA arms its own ready barrier for every response; the pair
@@ -606,6 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<CG>(tmem_base, TMEM_COLS);
+        if (lane == 0) TC_TRACE(p, 63);
     }
 }
 

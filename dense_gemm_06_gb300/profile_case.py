@@ -3,6 +3,7 @@
     python -m dense_gemm_06_gb300.profile_case --case sgemm --n 8192 --am 0 --bm 0 --reps 3
     python -m dense_gemm_06_gb300.profile_case --case bf16 --n 8192 --reps 3
     python -m dense_gemm_06_gb300.profile_case --case f16skinny --reps 3
+    python -m dense_gemm_06_gb300.profile_case --case f16small --reps 3
 
 Inputs are the seeded synthetic operands of the benchmark (datagen), resident
 on the device before the first launch; each repetition is one gemm() call on
@@ -27,6 +28,7 @@ CASES = {
     # name: (M, N, K, dtype, a_major, b_major, dist, seed, lo, hi)
     "sgemm": (8192, 8192, 8192, 0, 0, 0, "normal", 1027, 0, 0),
     "bf16": (8192, 8192, 8192, 4, 0, 0, "normal", 1028, 0, 0),
+    "f16small": (1024, 512, 256, 1, 0, 0, "int", 1025, -5, 5),
     "f16ragged": (4095, 3071, 1037, 1, 0, 1, "int", 1029, -3, 3),
     "f16skinny": (16384, 256, 8192, 1, 0, 1, "int", 1030, -3, 3),
     # 20 x 16 = 320 tiles of 128 x 128: a 16-tile last wave on 304 FFMA CTA slots
