@@ -31,6 +31,7 @@ GEMM_OPT_WAIT_LIMIT_NS, GEMM_OPT_TC_CTA_GROUP, GEMM_OPT_TC_FAULT_INJECT = 1, 2, 
 GEMM_OPT_SIMT_CONFIG, GEMM_OPT_SIMT_TRANSPOSE, GEMM_OPT_TC_STORE = 4, 5, 6
 GEMM_OPT_TC_MULTICAST, GEMM_OPT_SOFTMAX_FAULT_INJECT, GEMM_OPT_SIMT_SPLIT_TAIL = 7, 8, 9
 GEMM_OPT_TC_SCHEDULER, GEMM_OPT_SIMT_FAULT_INJECT = 10, 11
+GEMM_OPT_TC_TILE_N, GEMM_OPT_TC_SPLIT_TAIL = 12, 13
 GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_GELU = 0, 1, 2
 
 

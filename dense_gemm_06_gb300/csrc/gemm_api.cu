@@ -46,6 +46,8 @@ std::atomic<int> g_simt_fault_inject{0};
 std::atomic<int> g_tc_scheduler{0};
 std::atomic<int> g_tc_store{0};
 std::atomic<int> g_tc_multicast{0};
+std::atomic<int> g_tc_tile_n{0};
+std::atomic<int> g_tc_split{0};
 
 // The kernel configuration one call runs with. Every field is resolved
 // (no "automatic" values): an option set to a non-zero value wins, then a
@@ -58,6 +60,8 @@ struct RunConfig {
     int tc_store;        // 0 TMA where possible, 1 st.global
     int simt_split;      // 0 automatic K-split of the last wave, 1 never, 2 always
     int tc_scheduler;    // 1 static persistent, 2 cluster launch control
+    int tc_tile_n;       // 0 automatic, 64, 128, 256
+    int tc_split;        // 0 automatic, 1 never, 2 always
 };
 
 // Problems gemm_tune() has measured: shape, types, layouts and whether each
@@ -283,6 +287,8 @@ int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCon
     return rc;
 }
 
+TcLaunch tc_launch(const RunConfig& c);
+
 int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunConfig& cfg,
                cudaStream_t s) {
     if (p.K == 0) return zero_fill(p.C, p.M, p.N, p.ldc, out_bytes(p.dtype), dev, s);
@@ -318,10 +324,7 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCo
         if (cudaGetLastError() != cudaSuccess) rc = kCuda;
         else note_launch();
     }
-    if (rc == kOk)
-        rc = launch_gemm_tc(p, dev, cfg.cta_group, g_wait_limit_ns.load(),
-                            g_fault_inject.load(), cfg.tc_store != 1, cfg.multicast == 2,
-                            cfg.tc_scheduler == 2, s);
+    if (rc == kOk) rc = launch_gemm_tc(p, dev, tc_launch(cfg), s);
     for (int i = 0; i < 2; ++i)
         if (scratch[i]) cudaFreeAsync(scratch[i], s);
     return rc;
@@ -343,7 +346,7 @@ TuneKey make_key(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, in
 RunConfig resolve(const TuneKey& key) {
     RunConfig c{g_simt_config.load(), g_simt_transpose.load(), g_cta_group.load(),
                 g_tc_multicast.load(), g_tc_store.load(), g_simt_split.load(),
-                g_tc_scheduler.load()};
+                g_tc_scheduler.load(), g_tc_tile_n.load(), g_tc_split.load()};
     gemm_tuning t{};
     bool tuned = false;
     {
@@ -356,11 +359,19 @@ RunConfig resolve(const TuneKey& key) {
     }
     if (c.simt_config == 0) c.simt_config = tuned && t.simt_config ? t.simt_config : 9;
     if (c.simt_transpose == 0 && tuned) c.simt_transpose = t.simt_transpose;
-    if (c.cta_group == 0) c.cta_group = tuned && t.tc_cta_group ? t.tc_cta_group : 2;
+    // CTA group and tile width stay automatic (0) unless asked for or tuned:
+    // the launch picks them from the shape (plan_tc_shape)
+    if (c.cta_group == 0 && tuned) c.cta_group = t.tc_cta_group;
     c.multicast = c.multicast == 2 ? 2 : 1;  // only on request, never from a tuned entry
     if (c.tc_store == 0 && tuned) c.tc_store = t.tc_store;
     if (c.tc_scheduler == 0) c.tc_scheduler = tuned && t.tc_scheduler ? t.tc_scheduler : 1;
     return c;
+}
+
+TcLaunch tc_launch(const RunConfig& c) {
+    return TcLaunch{c.cta_group,         c.tc_tile_n,          c.tc_split,
+                    c.tc_store != 1,     c.multicast == 2,     c.tc_scheduler == 2,
+                    g_wait_limit_ns.load(), g_fault_inject.load()};
 }
 
 }  // namespace
@@ -422,16 +433,11 @@ int error_word_address(ErrWord** out) {
 
 ErrWord next_generation() { return g_generation.fetch_add(1, std::memory_order_relaxed); }
 
-uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
-int tc_fault_inject() { return g_fault_inject.load(); }
-
-TcOptions resolve_tc_options(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                             int a_major, const void* B, int64_t ldb, int b_major, const void* C,
-                             int64_t ldc, int c_major, int dtype) {
-    const RunConfig c =
-        resolve(make_key(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype));
-    return TcOptions{c.cta_group, c.tc_store != 1 ? 1 : 0, c.multicast == 2 ? 1 : 0,
-                     c.tc_scheduler == 2 ? 1 : 0};
+TcLaunch resolve_tc_options(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                            int a_major, const void* B, int64_t ldb, int b_major, const void* C,
+                            int64_t ldc, int c_major, int dtype) {
+    return tc_launch(
+        resolve(make_key(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc, c_major, dtype)));
 }
 
 int check_device_pointers(const void* const* ptrs, int n, int device) {
@@ -570,7 +576,8 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         // FFMA configurations 5 and 6 are sized for one CTA per SM, the others two
         const int ctas_per_sm = cfg.simt_config == 5 || cfg.simt_config == 6 ? 1 : 2;
         int64_t rows = host_panel_rows(pd.M, pd.N, pd.K, dtype == GEMM_F32, ctas_per_sm,
-                                       cfg.cta_group, cfg.multicast, dev->sm_count);
+                                       cfg.cta_group ? cfg.cta_group : 2, cfg.multicast,
+                                       dev->sm_count);
         if ((pd.M + rows - 1) / rows > kMaxPanels) rows = pd.M;
         const int np = (int)((pd.M + rows - 1) / rows);
 
@@ -895,6 +902,15 @@ int gemm_set_option(int option, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             g_simt_fault_inject.store((int)value);
             return GEMM_OK;
+        case GEMM_OPT_TC_TILE_N:
+            if (value != 0 && value != 64 && value != 128 && value != 256)
+                return GEMM_ERR_INVALID_ARG;
+            g_tc_tile_n.store((int)value);
+            return GEMM_OK;
+        case GEMM_OPT_TC_SPLIT_TAIL:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_tc_split.store((int)value);
+            return GEMM_OK;
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -912,6 +928,8 @@ int64_t gemm_get_option(int option) {
         case GEMM_OPT_SIMT_SPLIT_TAIL: return g_simt_split.load();
         case GEMM_OPT_TC_SCHEDULER: return g_tc_scheduler.load();
         case GEMM_OPT_SIMT_FAULT_INJECT: return g_simt_fault_inject.load();
+        case GEMM_OPT_TC_TILE_N: return g_tc_tile_n.load();
+        case GEMM_OPT_TC_SPLIT_TAIL: return g_tc_split.load();
         default: return -1;
     }
 }

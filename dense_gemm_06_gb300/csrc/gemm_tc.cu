@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "gemm_tc.cuh"
+#include "policy.h"
 
 namespace libgemm {
 namespace {
@@ -105,25 +106,31 @@ bool encode_tma_f32_2d(void* map, const float* ptr, uint64_t inner, uint64_t out
     return r == CUDA_SUCCESS;
 }
 
-int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
-                   uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled, int multicast,
-                   int clc, cudaStream_t stream) {
+int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, const TcLaunch& o,
+                   cudaStream_t stream) {
     if (!get_encoder()) return kCuda;
-    const int CG = cta_group == 1 ? 1 : 2;
-    const bool mc = CG == 2 && multicast;
+    const bool want_mc = o.cta_group != 1 && o.multicast;
+    const TcShape shape =
+        plan_tc_shape(pr.M, pr.N, o.cta_group, o.tile_n, want_mc, dev.sm_count);
+    const int CG = shape.cta_group;
+    const bool mc = CG == 2 && want_mc;
     const bool bf16 = pr.dtype == 2 || pr.dtype == 4;
     const int tile_m = ROWS_A * CG;
-    const int b_rows = TILE_N / CG;
 
     TcParams tp;
     std::memset(&tp, 0, sizeof(tp));
     // A: K-major -> dims {K, M}, box {64, 128}; M-major -> dims {M, K}, box {64, 64}.
-    // B likewise with its rows per CTA (64 per load when multicast).
+    // B K-major (dims {K, N}): a CTA's share of a tile (tile_n / CG rows) per
+    // box, and half that for half-width units; B N-major (dims {N, K}):
+    // 64-column boxes, as many as the CTA's share of the unit's width.
+    const uint32_t b_share = (uint32_t)(shape.tile_n / CG);
     bool ok = pr.a_kmajor
         ? encode_2d(&tp.tmap_a, bf16, pr.A, pr.K, pr.M, pr.lda, BK, ROWS_A)
         : encode_2d(&tp.tmap_a, bf16, pr.A, pr.M, pr.K, pr.lda, 64, BK);
     ok = ok && (pr.b_kmajor
-        ? encode_2d(&tp.tmap_b, bf16, pr.B, pr.K, pr.N, pr.ldb, BK, mc ? 64 : b_rows)
+        ? encode_2d(&tp.tmap_b, bf16, pr.B, pr.K, pr.N, pr.ldb, BK, mc ? 64 : b_share) &&
+              (mc || b_share < 128 ||
+               encode_2d(&tp.tmap_b_half, bf16, pr.B, pr.K, pr.N, pr.ldb, BK, b_share / 2))
         : encode_2d(&tp.tmap_b, bf16, pr.B, pr.N, pr.K, pr.ldb, 64, BK));
     if (!ok) return kCuda;
 
@@ -133,7 +140,7 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     tp.c_tma = 0;
     tp.epi = pr.epi;  // an active epilogue reads/stores C itself (no TMA store)
     if ((reinterpret_cast<uintptr_t>(pr.C) & 15u) == 0 && ((pr.ldc * out_bytes) & 15) == 0 &&
-        c_tma_enabled && !pr.epi.active) {
+        o.c_tma && !pr.epi.active) {
         const cuuint64_t dims[2] = {(cuuint64_t)pr.N, (cuuint64_t)pr.M};
         const cuuint64_t strides[1] = {(cuuint64_t)(pr.ldc * out_bytes)};
         const cuuint32_t box[2] = {32, 32};
@@ -153,20 +160,23 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, int cta_group,
     tp.M = (int)pr.M;
     tp.N = (int)pr.N;
     tp.K = (int)pr.K;
+    tp.tile_n = shape.tile_n;
     tp.tiles_m = (int)((pr.M + tile_m - 1) / tile_m);
-    tp.tiles_n = (int)((pr.N + TILE_N - 1) / TILE_N);
+    tp.tiles_n = (int)((pr.N + shape.tile_n - 1) / shape.tile_n);
+    tp.split_mode = o.split_mode;  // the split itself is planned at launch (resident clusters)
     tp.num_kb = (int)((pr.K + BK - 1) / BK);
     tp.c_vec = ((reinterpret_cast<uintptr_t>(pr.C) & 15u) == 0 &&
                 ((pr.ldc * out_bytes) & 15) == 0) ? 1 : 0;
     tp.err = dev.err_word;
     tp.gen = next_generation();
-    tp.wait_limit_ns = wait_limit_ns;
-    tp.fault_inject = fault_inject;
-    tp.clc = clc && !mc ? 1 : 0;  // the multicast variant keeps the static schedule
+    tp.wait_limit_ns = o.wait_limit_ns;
+    tp.fault_inject = o.fault_inject;
+    tp.clc = o.clc && !mc ? 1 : 0;  // the multicast variant keeps the static schedule
 #ifdef LIBGEMM_TC_TRACE
     tp.trace = g_trace;
 #endif
-    if ((int64_t)tp.tiles_m * tp.tiles_n * CG > 0x7fffffffLL) return kUnsupported;
+    // units (at most twice the tiles) x CTAs must fit the grid's int range
+    if ((int64_t)tp.tiles_m * tp.tiles_n * 2 * CG > 0x7fffffffLL) return kUnsupported;
 
     const bool a_mn = !pr.a_kmajor, b_mn = !pr.b_kmajor;
     switch (pr.dtype) {

@@ -15,19 +15,26 @@
 
 #include "epilogue.cuh"
 #include "internal.h"
+#include "policy.h"
 #include "ptx_sm100.cuh"
 
 namespace libgemm {
 
 struct TcParams {
     CUtensorMap tmap_a;
-    CUtensorMap tmap_b;
+    CUtensorMap tmap_b;        // K-major B: a CTA's whole share of a tile per box;
+                               // N-major B: 64-column boxes
+    CUtensorMap tmap_b_half;   // K-major B: the share of a half-width unit
     CUtensorMap tmap_c;        // valid when c_tma
     int c_tma;                 // C stored with TMA (16-byte aligned base and rows)
     void* C;
     int64_t ldc;
     int M, N, K;
     int tiles_m, tiles_n, num_kb;
+    int tile_n;                // columns of a tile: 256, 128 or 64 (>= 64 * CG)
+    int split_from;            // tiles from this raster index on run as two half-width
+                               // units (== tiles_m * tiles_n: none)
+    int split_mode;            // host only: GEMM_OPT_TC_SPLIT_TAIL, resolved at launch
     int c_vec;                 // C base / ldc allow 16-byte stores
     ErrWord* err;              // device error word
     ErrWord gen;               // this launch's generation (see internal.h)
@@ -73,7 +80,7 @@ using namespace gemm_ptx;
 
 constexpr int BK = 64;           // k per stage: 64 x 16-bit = one 128-byte swizzle row
 constexpr int UMMA_K = 16;       // k per tcgen05.mma (kind::f16)
-constexpr int TILE_N = 256;      // N per tile (per CTA pair when CG == 2)
+constexpr int TILE_N = 256;      // widest tile (per CTA pair when CG == 2): sizes the smem ring
 constexpr int ROWS_A = 128;      // A rows per CTA (= TMEM lanes)
 constexpr int ACC_COLS = 256;    // TMEM columns per accumulator
 constexpr int TMEM_COLS = 512;   // two accumulators
@@ -396,17 +403,35 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     const bool leader = rank == 0;
     const int cluster = CG == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
     const int nclusters = CG == 2 ? (int)num_clusters_x() : (int)gridDim.x;
-    // work units: tiles, or (MC) pairs of vertically adjacent tiles
+    // Tiles (or, MC, pairs of vertically adjacent tiles) in raster order; the
+    // tiles from split_from on are each run as two work units of half the
+    // width, so a last, partial round of tiles takes half as long.
     const int unit_rows = MC ? (p.tiles_m + 1) / 2 : p.tiles_m;
     const int total_tiles = unit_rows * p.tiles_n;
-    auto tile_of = [&](int t) {
-        TileCoord tc = raster(t, unit_rows, p.tiles_n);
-        if (MC) tc.tm = tc.tm * 2 + pair;  // may be past the last tile row: all rows OOB
-        return tc;
+    const int total_units = p.split_from + 2 * (total_tiles - p.split_from);
+    struct Unit {
+        int tm;     // tile row
+        int col0;   // first column of C
+        int width;  // columns (a multiple of 64 * CG)
     };
-    // Next tile of a role (t = total_tiles: no more work). Static schedule:
-    // every nclusters-th tile. CLC: the j-th response of the scheduler ring
-    // (the tile of a cluster it cancelled), which the role then releases to
+    auto unit_of = [&](int u) {
+        int t = u, off = 0, w = p.tile_n;
+        if (u >= p.split_from) {
+            const int v = u - p.split_from;
+            t = p.split_from + (v >> 1);
+            w = p.tile_n >> 1;
+            off = (v & 1) * w;
+        }
+        const TileCoord tc = raster(t, unit_rows, p.tiles_n);
+        Unit un;
+        un.tm = MC ? tc.tm * 2 + pair : tc.tm;  // MC: may be past the last tile row (all OOB)
+        un.col0 = tc.tn * p.tile_n + off;
+        un.width = w;
+        return un;
+    };
+    // Next unit of a role (t = total_units: no more work). Static schedule:
+    // every nclusters-th unit. CLC: the j-th response of the scheduler ring
+    // (the unit of a cluster it cancelled), which the role then releases to
     // the pair leader's consumed barrier. warp_wide: all lanes of the warp
     // call it and one arrives. False when a wait ran out.
     auto advance = [&](int& t, int& j, bool warp_wide) -> bool {
@@ -426,13 +451,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             else mbar_arrive_local(cons_bar(s));
         }
         ++j;
-        t = more ? x / CG : total_tiles;
+        t = more ? x / CG : total_units;
         return true;
     };
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&p.tmap_a);
         tma_prefetch_desc(&p.tmap_b);
+        if (!B_MN && p.split_from < total_tiles) tma_prefetch_desc(&p.tmap_b_half);
         for (int s = 0; s < C_::STAGES; ++s) {
             mbar_init(full_bar(s), 1);   // leader's producer arms it for both CTAs
             mbar_init(empty_bar(s), MC ? 2 : 1);  // MMA commits of every pair using the stage
@@ -468,15 +494,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             int j = 0;
-            for (int t = cluster; t < total_tiles && !aborted;) {
-                const TileCoord tc = tile_of(t);
-                const int a_row = tc.tm * C_::TILE_M + (int)rank * ROWS_A;
-                const int b_row = tc.tn * TILE_N + (int)rank * C_::B_ROWS;
+            for (int t = cluster; t < total_units && !aborted;) {
+                const Unit un = unit_of(t);
+                const int a_row = un.tm * C_::TILE_M + (int)rank * ROWS_A;
+                const int b_rows = un.width / CG;  // B rows (N) this CTA holds
+                const int b_row = un.col0 + (int)rank * b_rows;
+                // bytes both CTAs of the pair load per stage (OOB fill included)
+                const uint32_t bytes = (uint32_t)(CG * (C_::A_BYTES + b_rows * BK * 2));
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(empty_bar(stage), phase ^ 1u, p)) { aborted = true; break; }
                     const uint32_t fb =
                         CG == 2 ? mapa_shared(full_bar(stage), lead) : full_bar(stage);
-                    if (leader) mbar_arrive_expect_tx(full_bar(stage), CG * C_::STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes);
                     const uint32_t sa = sA0 + stage * C_::A_BYTES;
                     const uint32_t sb = sB0 + stage * C_::B_BYTES;
                     const int k0 = kb * BK;
@@ -497,11 +526,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                         else
                             tma_load_2d_mc_pair(dst, &p.tmap_b, fb, b_row + 64 * pair, k0, mask);
                     } else if constexpr (!B_MN) {
-                        tma_load_2d<CG>(sb, &p.tmap_b, fb, k0, b_row);
+                        // the CTA's rows of B in one box (fewer, larger boxes
+                        // measured faster: two 64-row boxes cost 4% at 8192^3)
+                        tma_load_2d<CG>(sb, un.width == p.tile_n ? &p.tmap_b : &p.tmap_b_half,
+                                        fb, k0, b_row);
                     } else {
-#pragma unroll
-                        for (int j = 0; j < C_::B_ROWS / 64; ++j)
-                            tma_load_2d<CG>(sb + j * 64 * BK * 2, &p.tmap_b, fb, b_row + 64 * j, k0);
+                        // 64-column boxes (the width of the 128-byte swizzle)
+                        for (int j = 0; j < b_rows / 64; ++j)
+                            tma_load_2d<CG>(sb + j * 64 * BK * 2, &p.tmap_b, fb,
+                                            b_row + 64 * j, k0);
                     }
                     if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -513,15 +546,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
         if (leader && lane == 0) {
-            constexpr uint32_t idesc =
-                make_idesc_f16(BF16, A_MN, B_MN, (uint32_t)C_::TILE_M, (uint32_t)TILE_N);
+            // instruction descriptor without N (bits 17-22 = N >> 3, per unit)
+            constexpr uint32_t idesc0 =
+                make_idesc_f16(BF16, A_MN, B_MN, (uint32_t)C_::TILE_M, 0u);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             int j = 0;
-            int nt = 0;  // tiles issued (trace slots)
-            for (int t = cluster; t < total_tiles && !aborted;) {
+            int nt = 0;  // units issued (trace slots)
+            for (int t = cluster; t < total_units && !aborted;) {
+                const uint32_t idesc = idesc0 | ((uint32_t)(unit_of(t).width >> 3) << 17);
                 if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, p)) { aborted = true; break; }
                 tc_fence_after_sync();
                 TC_TRACE(p, 4 + 4 * nt);
@@ -579,26 +614,26 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             if (!__all_sync(0xffffffffu, wait_bar(never_bar, 0u, p))) aborted = true;
         }
         int j = 0;
-        int nt = 0;  // tiles stored (trace slots)
-        for (int t = cluster; t < total_tiles && !aborted;) {
-            const TileCoord tc = tile_of(t);
+        int nt = 0;  // units stored (trace slots)
+        for (int t = cluster; t < total_units && !aborted;) {
+            const Unit un = unit_of(t);
             if (!__all_sync(0xffffffffu, wait_bar(accf_bar(acc), acc_phase, p))) {
                 aborted = true;
                 break;
             }
             tc_fence_after_sync();
             if (warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 6 + 4 * nt);
-            const int row0 = tc.tm * C_::TILE_M + (int)rank * ROWS_A + q * 32;
+            const int row0 = un.tm * C_::TILE_M + (int)rank * ROWS_A + q * 32;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             const uint32_t stage = epi0 + (uint32_t)((warp - EPI_WARP0) * 32 * 128);
 #pragma unroll 1
-            for (int c = half; c < ACC_COLS / 32; c += 2) {
+            for (int c = half; c < un.width / 32; c += 2) {
                 uint32_t v[32];
                 if (nt == 0 && warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 20 + 4 * c);
                 tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
                 tmem_wait_ld();
                 if (nt == 0 && warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 21 + 4 * c);
-                store_chunk<OutT>(p, stage, lane, row0, tc.tn * TILE_N + c * 32, v);
+                store_chunk<OutT>(p, stage, lane, row0, un.col0 + c * 32, v);
                 if (nt == 0 && warp == EPI_WARP0 && lane == 0) TC_TRACE(p, 22 + 4 * c);
             }
             tc_fence_before_sync();
@@ -696,8 +731,11 @@ int launch_variant(TcParams& tp, const DeviceInfo& dev, cudaStream_t stream) {
         }
     }
     const int unit_rows = MC ? (tp.tiles_m + 1) / 2 : tp.tiles_m;
-    const int total = unit_rows * tp.tiles_n;
-    // persistent: as many clusters as fit at once; CLC: one cluster per tile
+    const int tiles = unit_rows * tp.tiles_n;
+    tp.split_from = (int)plan_tc_split(tiles, max_clusters[dev.device & 63], tp.tile_n, CG, MC,
+                                       tp.split_mode);
+    const int total = tp.split_from + 2 * (tiles - tp.split_from);  // work units
+    // persistent: as many clusters as fit at once; CLC: one cluster per unit
     int nclusters = tp.clc ? total : max_clusters[dev.device & 63];
     if (nclusters > total) nclusters = total;
     if (nclusters < 1) nclusters = 1;

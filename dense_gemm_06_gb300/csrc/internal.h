@@ -97,14 +97,21 @@ bool encode_tma_f32_2d(void* map, const float* ptr, uint64_t inner, uint64_t out
 // dst[c * ldd + r] = src[r * lds + c] (fp32), rows x cols.
 int launch_transpose_f32(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
                          int64_t cols, const DeviceInfo& dev, cudaStream_t stream);
-// c_tma_enabled: 1 = store C with TMA when its rows are 16-byte aligned,
-// 0 = always use the st.global epilogue. multicast: 1 = clusters of two CTA
-// pairs sharing B through TMA multicast (2-CTA mode only).
-// clc: 1 = one cluster per tile, running clusters take over unstarted ones
-// with cluster launch control (try_cancel); 0 = persistent static schedule.
-int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, int cta_group,
-                   uint64_t wait_limit_ns, int fault_inject, int c_tma_enabled, int multicast,
-                   int clc, cudaStream_t stream);
+// How one tensor-core launch runs (every field resolved except where 0 means
+// automatic; the shape rules are plan_tc_shape / plan_tc_split in policy.h).
+struct TcLaunch {
+    int cta_group;   // 0 automatic, 1 a CTA per tile, 2 a CTA pair per tile
+    int tile_n;      // 0 automatic, or 64, 128, 256 columns per tile
+    int split_mode;  // last-round split into half-width units: 0 auto, 1 never, 2 always
+    int c_tma;       // 1: TMA stores of C where its rows are 16-byte aligned; 0: st.global
+    int multicast;   // 1: clusters of two CTA pairs sharing B through TMA multicast
+    int clc;         // 1: one cluster per unit, cluster launch control takes over
+                     // unstarted ones; 0: persistent static schedule
+    uint64_t wait_limit_ns;
+    int fault_inject;  // test hook (GEMM_OPT_TC_FAULT_INJECT)
+};
+int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, const TcLaunch& o,
+                   cudaStream_t stream);
 
 void note_launch(uint64_t n = 1);
 
@@ -123,20 +130,11 @@ int error_word_address(ErrWord** out);
 // launch, so no kernel -- in particular no cluster-multicast TMA load -- ever
 // addresses another GPU's memory.
 int check_device_pointers(const void* const* ptrs, int n, int device);
-// The tensor-core kernel options gemm() resolves for a problem: an option the
+// The tensor-core launch options gemm() resolves for a problem: an option the
 // caller set wins, then a gemm_tune() entry for the problem, then the default.
-struct TcOptions {
-    int cta_group;  // 1 or 2
-    int c_tma;      // 1: TMA stores where C allows, 0: st.global only
-    int multicast;  // 1: B multicast across two pairs (only when the option asks)
-    int clc;        // 1: cluster-launch-control scheduler
-};
-TcOptions resolve_tc_options(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                             int a_major, const void* B, int64_t ldb, int b_major, const void* C,
-                             int64_t ldc, int c_major, int dtype);
-// The GEMM_OPT_WAIT_LIMIT_NS and GEMM_OPT_TC_FAULT_INJECT values.
-uint64_t wait_limit_ns();
-int tc_fault_inject();
+TcLaunch resolve_tc_options(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                            int a_major, const void* B, int64_t ldb, int b_major, const void* C,
+                            int64_t ldc, int c_major, int dtype);
 
 // Row softmax over thread-block clusters (softmax_cluster.cu); rows longer
 // than softmax_max_cols() are not supported.

@@ -1,8 +1,9 @@
 // policy.h -- the host-side choices the library makes automatically, as plain
 // C++ (no CUDA), so they can be compiled and checked on a machine without a
 // GPU: the FFMA kernel's K-split of the tiles left after its last full round,
-// whether a K-major fp32 operand is first transposed, and the row panels
-// gemm_host() pipelines its copies over.
+// whether a K-major fp32 operand is first transposed, the row panels
+// gemm_host() pipelines its copies over, and the tensor-core kernel's tile
+// shape and split of its last round.
 #pragma once
 
 #include <cstdint>
@@ -98,6 +99,65 @@ inline int64_t host_panel_rows(int64_t M, int64_t N, int64_t K, bool f32, int ct
     int64_t r = slots / std::gcd(slots, tiles_n);
     while (r * 8 < tiles_m) r *= 2;
     return r >= tiles_m ? M : r * tm;
+}
+
+// Tensor-core tile shape: the CTA group (1: a CTA per 128-row tile, 2: a
+// CTA pair per 256-row tile) and the tile width in columns (64, 128 or 256;
+// at least 64 per CTA of the group). cta_group / tile_n: the value asked for,
+// or 0 for automatic. Automatic: a problem with fewer 256 x 256 pair tiles
+// than a quarter of the SMs (fewer than half the CTA pairs would get one)
+// runs one CTA per tile, in the narrowest width that still fits every tile
+// into one round over the SMs, so its epilogue (the part of a short problem
+// that takes longest) is spread over as many SMs as possible; everything
+// else runs 256 x 256 pair tiles. Operand multicast always runs 256 x 256
+// pair tiles.
+struct TcShape {
+    int cta_group;
+    int tile_n;
+};
+
+inline TcShape plan_tc_shape(int64_t M, int64_t N, int cta_group, int tile_n, bool multicast,
+                             int sm_count) {
+    TcShape s{cta_group, tile_n};
+    if (multicast) return TcShape{2, 256};
+    if (s.cta_group != 1 && s.cta_group != 2) {
+        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+        s.cta_group = pair_tiles * 4 < (int64_t)sm_count ? 1 : 2;
+    }
+    if (s.tile_n != 64 && s.tile_n != 128 && s.tile_n != 256) {
+        s.tile_n = 256;
+        if (s.cta_group == 1)
+            for (int tn = 64; tn < 256; tn *= 2)
+                if (((M + 127) / 128) * ((N + tn - 1) / tn) <= (int64_t)sm_count) {
+                    s.tile_n = tn;
+                    break;
+                }
+    }
+    if (s.tile_n < 64 * s.cta_group) s.tile_n = 64 * s.cta_group;
+    return s;
+}
+
+// The first tile (raster order) of a tensor-core launch that runs as two
+// work units of half the width. With `slots` clusters resident at once and T
+// tiles, the last round holds r = T mod slots tiles; when at least two rounds
+// are needed and r is at most half the slots, splitting those r tiles makes
+// the last round take half as long (2 r half units still fit in one round):
+// at 8192^3 (1024 pair tiles on 76 pairs, r = 36) 14 rounds become 13.5.
+// split_mode 0: automatic; 1: never; 2 (tests): split the last round's
+// tiles (every tile when there is less than one round) whatever it saves.
+// Half units need half the width to hold 64 columns per CTA; operand
+// multicast never splits. Returns T for no split.
+inline int64_t plan_tc_split(int64_t T, int64_t slots, int tile_n, int cta_group,
+                             bool multicast, int split_mode) {
+    if (split_mode == 1 || multicast || tile_n / 2 < 64 * cta_group || slots <= 0 || T <= 0)
+        return T;
+    int64_t r = T % slots;
+    if (split_mode == 2) {
+        if (r == 0) r = T < slots ? T : slots;
+        return T - r;
+    }
+    if (T <= slots || r == 0 || 2 * r > slots) return T;
+    return T - r;
 }
 
 }  // namespace libgemm

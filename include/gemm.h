@@ -291,9 +291,11 @@ enum gemm_option {
        A wait that runs past it records GEMM_ERR_TIMEOUT in the device error
        word and the kernel winds down without further writes to C. */
     GEMM_OPT_WAIT_LIMIT_NS = 1,
-    /* Tensor-core kernel variant: 0 = automatic (the 2-CTA pair kernel),
-       1 = one CTA per tile (cta_group::1, 128 x 256 tiles),
-       2 = CTA pair per tile (cta_group::2, 256 x 256 tiles). */
+    /* Tensor-core kernel variant: 0 = automatic (the 2-CTA pair kernel, or
+       one CTA per tile for problems with fewer 256 x 256 tiles than a quarter
+       of the SMs; see GEMM_OPT_TC_TILE_N),
+       1 = one CTA per tile (cta_group::1, 128-row tiles),
+       2 = CTA pair per tile (cta_group::2, 256-row tiles). */
     GEMM_OPT_TC_CTA_GROUP = 2,
     /* Test hook for the timeout path: 1 makes the tensor-core kernel's
        epilogue wait on a barrier that nothing completes, so every call times
@@ -365,7 +367,20 @@ enum gemm_option {
        first CTA skip the copy of its second k-tile, so that CTA's waits run
        out after GEMM_OPT_WAIT_LIMIT_NS and gemm_check_device_error reports
        GEMM_ERR_TIMEOUT; C is then undefined. 0 (default) = off. */
-    GEMM_OPT_SIMT_FAULT_INJECT = 11
+    GEMM_OPT_SIMT_FAULT_INJECT = 11,
+    /* Tile width of the tensor-core kernel in columns of C: 0 = automatic
+       (256; a problem with fewer 256 x 256 tiles than a quarter of the SMs
+       runs one CTA per tile, in the narrowest of 64 / 128 / 256 columns that
+       still fits every tile into one round over the SMs), or 64, 128, 256
+       (at least 64 per CTA: a CTA pair needs 128 or 256). Operand multicast
+       always uses 256. */
+    GEMM_OPT_TC_TILE_N = 12,
+    /* Last round of the tensor-core kernel: 0 = automatic (when a launch
+       takes at least two rounds of tiles over its resident clusters and the
+       last round is at most half full, each of its tiles runs as two work
+       units of half the width, so that round takes half as long), 1 = never,
+       2 = always split the last round's tiles (tests). */
+    GEMM_OPT_TC_SPLIT_TAIL = 13
 };
 
 /* gemm_set_option -- set an option; GEMM_OK or GEMM_ERR_INVALID_ARG. */

@@ -108,7 +108,8 @@ def make_operands(M, N, K, dtype, a_major, b_major, dist, seed, lda_pad=0, ldb_p
 
 
 def run_device_gemm(M, N, K, dtype, A, lda, a_major, B, ldb, b_major, c_major=1, ldc_pad=0,
-                    cta_group=0, dA=None, dB=None, tc_store=0, multicast=0, scheduler=0):
+                    cta_group=0, dA=None, dB=None, tc_store=0, multicast=0, scheduler=0,
+                    tile_n=0, split=0):
     """Runs gemm() through the C ABI; returns the logical C (float64)."""
     torch = torch_mod()
     ot = lg.OUT_TYPE[dtype]
@@ -122,6 +123,10 @@ def run_device_gemm(M, N, K, dtype, A, lda, a_major, B, ldb, b_major, c_major=1,
     old_store = lg.gemm_get_option(lg.GEMM_OPT_TC_STORE)
     old_mc = lg.gemm_get_option(lg.GEMM_OPT_TC_MULTICAST)
     old_sched = lg.gemm_get_option(lg.GEMM_OPT_TC_SCHEDULER)
+    old_tile = lg.gemm_get_option(lg.GEMM_OPT_TC_TILE_N)
+    old_split = lg.gemm_get_option(lg.GEMM_OPT_TC_SPLIT_TAIL)
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_TILE_N, tile_n), "set_option")
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_SPLIT_TAIL, split), "set_option")
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_CTA_GROUP, cta_group), "set_option")
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_STORE, tc_store), "set_option")
     lg.check(lg.gemm_set_option(lg.GEMM_OPT_TC_MULTICAST, multicast), "set_option")
@@ -137,6 +142,8 @@ def run_device_gemm(M, N, K, dtype, A, lda, a_major, B, ldb, b_major, c_major=1,
         lg.gemm_set_option(lg.GEMM_OPT_TC_STORE, old_store)
         lg.gemm_set_option(lg.GEMM_OPT_TC_MULTICAST, old_mc)
         lg.gemm_set_option(lg.GEMM_OPT_TC_SCHEDULER, old_sched)
+        lg.gemm_set_option(lg.GEMM_OPT_TC_TILE_N, old_tile)
+        lg.gemm_set_option(lg.GEMM_OPT_TC_SPLIT_TAIL, old_split)
     return cbuf.read()
 
 

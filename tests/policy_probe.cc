@@ -5,6 +5,8 @@
 //   split  T slots sm_count nkt mode      -> "dp_tiles splits kt_slice"
 //   transpose other M N K mode            -> "0" or "1"
 //   panel  M N K f32 ctas_per_sm cta_group multicast sm_count -> "rows"
+//   tcshape M N cta_group tile_n multicast sm_count         -> "cta_group tile_n"
+//   tcsplit T slots tile_n cta_group multicast mode          -> "split_from"
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -32,6 +34,18 @@ int main(int argc, char** argv) {
                                                arg(argv, 5) != 0, (int)arg(argv, 6),
                                                (int)arg(argv, 7), (int)arg(argv, 8),
                                                (int)arg(argv, 9)));
+        return 0;
+    }
+    if (argc >= 8 && std::strcmp(argv[1], "tcshape") == 0) {
+        const TcShape t = plan_tc_shape(arg(argv, 2), arg(argv, 3), (int)arg(argv, 4),
+                                        (int)arg(argv, 5), arg(argv, 6) != 0, (int)arg(argv, 7));
+        std::printf("%d %d\n", t.cta_group, t.tile_n);
+        return 0;
+    }
+    if (argc >= 8 && std::strcmp(argv[1], "tcsplit") == 0) {
+        std::printf("%lld\n", (long long)plan_tc_split(arg(argv, 2), arg(argv, 3),
+                                                        (int)arg(argv, 4), (int)arg(argv, 5),
+                                                        arg(argv, 6) != 0, (int)arg(argv, 7)));
         return 0;
     }
     std::fprintf(stderr, "usage: see the header of policy_probe.cc\n");

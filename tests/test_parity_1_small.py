@@ -40,16 +40,18 @@ def rne16(x: np.ndarray, t: str) -> np.ndarray:
 # tensor-core kernel modes: (CTA group, operand multicast across two pairs,
 # tile scheduler: 1 static persistent, 2 cluster launch control)
 TC_MODES = {"cg1": (1, 1, 1), "cg2": (2, 1, 1), "cg2mc": (2, 2, 1), "cg1clc": (1, 1, 2),
-            "cg2clc": (2, 1, 2)}
+            "cg2clc": (2, 1, 2), "auto": (0, 0, 0)}
 
 
 def run_and_check(M, N, K, dtype, am, bm, cm=1, dist="int", seed=0, lda_pad=0, ldb_pad=0,
-                  ldc_pad=0, cta_group=0, tc_store=0, multicast=0, scheduler=0):
+                  ldc_pad=0, cta_group=0, tc_store=0, multicast=0, scheduler=0, tile_n=0,
+                  split=0):
     A, lda, B, ldb = make_operands(M, N, K, dtype, am, bm, dist, seed, lda_pad, ldb_pad)
     C = run_device_gemm(M, N, K, dtype, A, lda, am, B, ldb, bm, cm, ldc_pad, cta_group,
-                        tc_store=tc_store, multicast=multicast, scheduler=scheduler)
+                        tc_store=tc_store, multicast=multicast, scheduler=scheduler,
+                        tile_n=tile_n, split=split)
     what = (f"{M}x{N}x{K} dtype={dtype} A{'KM'[am]} B{'KN'[bm]} C{'MN'[cm]} cg={cta_group} "
-            f"store={tc_store} mc={multicast} sched={scheduler}")
+            f"store={tc_store} mc={multicast} sched={scheduler} tile_n={tile_n} split={split}")
     ot = lg.OUT_TYPE[dtype]
     if dist == "int" and ot != "f32":
         import oracle
@@ -133,6 +135,29 @@ def test_tc_many_tiles_per_cta(mode):
                   cta_group=cg, multicast=mc, scheduler=sch)
     run_and_check(2816, 1280, 200, lg.GEMM_BF16_F32, 1, 1, 1, dist="int", seed=10,
                   cta_group=cg, multicast=mc, scheduler=sch)
+
+
+@pytest.mark.parametrize("split", [1, 2])
+@pytest.mark.parametrize("sched", [1, 2])
+@pytest.mark.parametrize("cg,tile_n", [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("am,bm", list(itertools.product((0, 1), (0, 1))))
+def test_tc_tile_widths_and_split_units(am, bm, cg, tile_n, sched, split):
+    # every tile width, with the last round's tiles run whole (split 1) or as
+    # two half-width units (split 2; every tile here, under one round), under
+    # both tile schedulers; ragged M, N and K
+    run_and_check(777, 1000, 333, lg.GEMM_F16_F32, am, bm, 1, dist="int", seed=11,
+                  cta_group=cg, scheduler=sched, tile_n=tile_n, split=split)
+    run_and_check(333, 650, 130, lg.GEMM_BF16_BF16, am, bm, 0, dist="normal", seed=12,
+                  cta_group=cg, scheduler=sched, tile_n=tile_n, split=split)
+
+
+@pytest.mark.parametrize("cg,tile_n", [(1, 128), (2, 256)])
+def test_tc_split_last_round_of_many(cg, tile_n):
+    # more tiles than resident clusters: the last round's tiles run as half
+    # units after whole tiles (auto and forced), int data compared exactly
+    for split in (0, 2):
+        run_and_check(4736, 2304, 192, lg.GEMM_F16_F32, 0, 1, 1, dist="int", seed=13,
+                      cta_group=cg, tile_n=tile_n, split=split)
 
 
 # ----------------------------------------------------- degenerate sizes --

@@ -1,7 +1,8 @@
 """The library's automatic host-side choices, checked on the CPU: the FFMA
 kernel's K-split of the tiles after its last full round (the per-SM model),
-the transpose rule for K-major fp32 operands, and the row panels that
-gemm_host() pipelines its copies over. tests/policy_probe.cc is compiled with
+the transpose rule for K-major fp32 operands, the row panels that
+gemm_host() pipelines its copies over, and the tensor-core kernel's tile
+shape and last-round split. tests/policy_probe.cc is compiled with
 the host C++ compiler against the library's own policy header, so these are
 the choices the library makes; the expected values are the outcomes the
 model gives by hand for a 152-SM GB300 (two FFMA CTAs per SM), including the
@@ -100,3 +101,49 @@ def test_host_panels(probe):
     # too small to pipeline (M N K < 1e10), or nothing to multiply
     assert probe("panel", 2048, 2048, 2048, 1, 2, 2, 1, P) == 2048
     assert probe("panel", 8192, 8192, 0, 1, 2, 2, 1, P) == 8192
+
+
+@pytest.mark.parametrize("M,N,cg,tn,mc,want", [
+    # 1024 x 512: 8 pair tiles < 152 / 4 -> one CTA per tile, 8 x 8 tiles of 64
+    (1024, 512, 0, 0, 0, (1, 64)),
+    # 16 x 16 pair tiles >= 38: CTA pairs, 256 wide
+    (4096, 4096, 0, 0, 0, (2, 256)),
+    # the ragged fp16 problem (16 x 12 pair tiles) and the skinny one (64)
+    (4095, 3071, 0, 0, 0, (2, 256)),
+    (16384, 256, 0, 0, 0, (2, 256)),
+    # 37 pair tiles (37 x 4 < 152): one CTA per tile; 74 row tiles x 4 of 64
+    # columns would not fit one round over 152 SMs, x 2 of 128 do (148)
+    (256 * 37, 256, 0, 0, 0, (1, 128)),
+    # 74 pair tiles (296 >= 152): CTA pairs
+    (128 * 74, 512, 0, 0, 0, (2, 256)),
+    # forced values win; a pair needs 128 columns at least; multicast is 2 x 256
+    (1024, 512, 2, 0, 0, (2, 256)),
+    (1024, 512, 2, 64, 0, (2, 128)),
+    (8192, 8192, 1, 0, 0, (1, 256)),
+    (8192, 8192, 0, 128, 0, (2, 128)),
+    (1024, 512, 1, 0, 1, (2, 256)),
+])
+def test_tc_shape(probe, M, N, cg, tn, mc, want):
+    assert probe("tcshape", M, N, cg, tn, mc, P) == want
+
+
+def test_tc_split(probe):
+    # bf16 8192^3: 1024 pair tiles on 76 pairs, last round 36 <= 38 -> split
+    assert probe("tcsplit", 1024, 76, 256, 2, 0, 0) == 988
+    # ragged fp16: 192 tiles, last round 40 > 38 -> no gain, no split
+    assert probe("tcsplit", 192, 76, 256, 2, 0, 0) == 192
+    # one round or less, a whole number of rounds: no split
+    assert probe("tcsplit", 64, 76, 256, 2, 0, 0) == 64
+    assert probe("tcsplit", 152, 76, 256, 2, 0, 0) == 152
+    # half units must keep 64 columns per CTA; multicast never splits
+    assert probe("tcsplit", 1024, 76, 128, 2, 0, 0) == 1024
+    assert probe("tcsplit", 1024, 76, 256, 2, 1, 0) == 1024
+    assert probe("tcsplit", 400, 152, 128, 1, 0, 0) == 400   # 96 in the last round > 76
+    assert probe("tcsplit", 350, 152, 128, 1, 0, 0) == 304   # 46 in the last round
+    # never / forced (tests: the last round, or every tile under one round)
+    assert probe("tcsplit", 1024, 76, 256, 2, 0, 1) == 1024
+    assert probe("tcsplit", 192, 76, 256, 2, 0, 2) == 152
+    assert probe("tcsplit", 8, 76, 256, 2, 0, 2) == 0
+    assert probe("tcsplit", 152, 76, 256, 2, 0, 2) == 76
+    # occupancy unknown: never
+    assert probe("tcsplit", 1024, 0, 256, 2, 0, 0) == 1024
