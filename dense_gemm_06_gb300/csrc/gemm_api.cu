@@ -295,38 +295,47 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCo
     if (p.dtype == GEMM_F32) return run_sgemm(p, dev, pool, cfg, s);
 
     // Tensor-core path: TMA needs 16-byte aligned bases and row pitches.
-    void* scratch[2] = {nullptr, nullptr};
+    // Misaligned operands are repacked into one scratch allocation (each
+    // operand's part 256-byte aligned), in one launch.
+    void* scratch = nullptr;
     int rc = kOk;
     const void** ops[2] = {&p.A, &p.B};
     int64_t* lds[2] = {&p.lda, &p.ldb};
     const bool kmaj[2] = {p.a_kmajor, p.b_kmajor};
     const int64_t rows[2] = {p.M, p.N};
     Repack16 job[2] = {};  // outer == 0: nothing to repack
-    for (int i = 0; i < 2 && rc == kOk; ++i) {
+    int64_t off[2] = {0, 0}, bytes = 0;
+    for (int i = 0; i < 2; ++i) {
         if (tma_ok(*ops[i], *lds[i], 2)) continue;
         const int64_t inner = kmaj[i] ? p.K : rows[i];
         const int64_t outer = kmaj[i] ? rows[i] : p.K;
         const int64_t ld2 = round_up(inner, 8);
-        if (cudaMallocFromPoolAsync(&scratch[i], (size_t)(outer * ld2 * 2), pool, s) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            rc = kCuda;
-            break;
-        }
-        job[i] = {static_cast<const uint16_t*>(*ops[i]), static_cast<uint16_t*>(scratch[i]),
-                  *lds[i], ld2, outer, inner};
-        *ops[i] = scratch[i];
-        *lds[i] = ld2;
+        job[i] = {static_cast<const uint16_t*>(*ops[i]), nullptr, *lds[i], ld2, outer, inner};
+        off[i] = bytes;
+        bytes += round_up(outer * ld2 * 2, 256);
     }
-    if (rc == kOk && job[0].outer + job[1].outer > 0) {  // both operands in one launch
+    if (bytes > 0) {
+        if (cudaMallocFromPoolAsync(&scratch, (size_t)bytes, pool, s) != cudaSuccess) {
+            cudaGetLastError();
+            return kCuda;
+        }
+        for (int i = 0; i < 2; ++i) {
+            if (job[i].outer == 0) continue;
+            job[i].dst = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + off[i]);
+            *ops[i] = job[i].dst;
+            *lds[i] = job[i].ldd;
+        }
         repack16_kernel<<<repack16_blocks(job[0].outer + job[1].outer, dev.sm_count), 256, 0,
                           s>>>(job[0], job[1]);
         if (cudaGetLastError() != cudaSuccess) rc = kCuda;
         else note_launch();
     }
-    if (rc == kOk) rc = launch_gemm_tc(p, dev, tc_launch(cfg), s);
-    for (int i = 0; i < 2; ++i)
-        if (scratch[i]) cudaFreeAsync(scratch[i], s);
+    if (rc == kOk) {
+        TcLaunch o = tc_launch(cfg);
+        o.after_repack = bytes > 0 ? 1 : 0;
+        rc = launch_gemm_tc(p, dev, o, s);
+    }
+    if (scratch) cudaFreeAsync(scratch, s);
     return rc;
 }
 
@@ -371,7 +380,7 @@ RunConfig resolve(const TuneKey& key) {
 TcLaunch tc_launch(const RunConfig& c) {
     return TcLaunch{c.cta_group,         c.tc_tile_n,          c.tc_split,
                     c.tc_store != 1,     c.multicast == 2,     c.tc_scheduler == 2,
-                    g_wait_limit_ns.load(), g_fault_inject.load()};
+                    g_wait_limit_ns.load(), g_fault_inject.load(), 0};
 }
 
 }  // namespace

@@ -169,8 +169,9 @@ extern "C" int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int6
         }
         // The same kernel options gemm() would resolve for this problem
         // (caller's options, then a gemm_tune() entry, then the default).
-        const TcLaunch o = resolve_tc_options(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc,
-                                              c_major, dtype);
+        TcLaunch o = resolve_tc_options(M, N, K, A, lda, a_major, B, ldb, b_major, C, ldc,
+                                        c_major, dtype);
+        o.after_repack = rows_all > 0 ? 1 : 0;
         return launch_gemm_tc(p, fd->info, o, s);
     } catch (...) {
         return kCuda;

@@ -35,6 +35,8 @@ struct TcParams {
     int split_from;            // tiles from this raster index on run as two half-width
                                // units (== tiles_m * tiles_n: none)
     int split_mode;            // host only: GEMM_OPT_TC_SPLIT_TAIL, resolved at launch
+    int pdl;                   // host only: launched as a programmatic dependent of the
+                               // repack kernel before it on the stream
     int c_vec;                 // C base / ldc allow 16-byte stores
     ErrWord* err;              // device error word
     ErrWord gen;               // this launch's generation (see internal.h)
@@ -491,6 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
+            pdl_wait();  // operands written by the kernel before this one (repack)
             int stage = 0;
             uint32_t phase = 0;
             int j = 0;
@@ -607,6 +610,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         const int half = (warp - EPI_WARP0) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
+        pdl_wait();  // C may be read (fused epilogue) or written only after earlier kernels
         // Every lane waits; the decision to go on is taken warp-uniformly
         // (__all_sync) because tcgen05.ld below is a .sync.aligned warp op.
         if (p.fault_inject == 1) {
@@ -741,8 +745,13 @@ int launch_variant(TcParams& tp, const DeviceInfo& dev, cudaStream_t stream) {
     if (nclusters < 1) nclusters = 1;
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cluster_cfg(cfg, attr, nclusters);
+    if (tp.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     cfg.stream = stream;
     if (cudaLaunchKernelEx(&cfg, kern, tp) != cudaSuccess) return kCuda;
     note_launch();

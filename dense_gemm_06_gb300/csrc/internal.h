@@ -109,6 +109,8 @@ struct TcLaunch {
                      // unstarted ones; 0: persistent static schedule
     uint64_t wait_limit_ns;
     int fault_inject;  // test hook (GEMM_OPT_TC_FAULT_INJECT)
+    int after_repack;  // 1: the previous launch on the stream is this call's repack
+                       // kernel: launch as its programmatic dependent
 };
 int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, const TcLaunch& o,
                    cudaStream_t stream);

@@ -108,6 +108,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// The next kernel of the stream, if it was launched with programmatic stream
+// serialization, may start before this grid has completed.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their memory
+// writes are visible; returns at once for a kernel launched without
+// programmatic stream serialization.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {

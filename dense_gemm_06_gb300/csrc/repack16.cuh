@@ -14,6 +14,8 @@
 
 #include <cstdint>
 
+#include "ptx_sm100.cuh"
+
 namespace libgemm {
 namespace {
 
@@ -72,6 +74,9 @@ __device__ __forceinline__ void repack16_row(const uint16_t* __restrict__ src,
 // Repacks up to two operands in one launch: warp w of the grid takes rows w,
 // w + (warps in the grid), ... of a's rows followed by b's.
 __global__ void __launch_bounds__(256) repack16_kernel(const Repack16 a, const Repack16 b) {
+    // the GEMM launched after this may set itself up meanwhile (it waits for
+    // this grid to complete before it reads the repacked rows)
+    gemm_ptx::pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     const int64_t rows = a.outer + b.outer;
