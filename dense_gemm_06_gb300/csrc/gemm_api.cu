@@ -900,7 +900,7 @@ int gemm_set_option(int option, int64_t value) {
             g_softmax_fault_inject.store((int)value);
             return GEMM_OK;
         case GEMM_OPT_SIMT_SPLIT_TAIL:
-            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
             g_simt_split.store((int)value);
             return GEMM_OK;
         case GEMM_OPT_TC_SCHEDULER:

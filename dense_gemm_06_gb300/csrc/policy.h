@@ -65,6 +65,45 @@ inline TailSplit plan_tail_split(int64_t T, int slots, int sm_count, int nkt, in
     return t;
 }
 
+// Stream-K plan of the TMA-fed FFMA kernel: tiles 0 .. dp_tiles-1 (raster
+// order) run whole, one CTA each; the k-iterations of the later tiles (tile
+// t, k-tile k is iteration (t - dp_tiles) * nkt + k) are shared evenly by
+// sk_ctas CTAs, each taking one contiguous range (at most one tile's worth,
+// so at most two tile segments). sk_ctas == 0: no stream-K.
+struct StreamK {
+    int dp_tiles;
+    int sk_ctas;
+};
+
+// Model: with P SMs, `slots` = 2 P resident CTAs (two per SM) and
+// P <= T < 2 P tiles, whole tiles give some SMs two tiles, so the launch
+// takes two tiles' time. Sharing every tile's k-iterations evenly over all
+// `slots` CTAs gives every CTA, wherever the block scheduler places it, the
+// same T / (2 P) tiles' worth, so every SM does T / P: split_mode 0
+// (automatic) uses that when it saves at least 10% (T <= 1.8 P) and a tile
+// has at least 32 k-tiles. (Mixing whole-tile CTAs with stream-K CTAs
+// measured slower: co-resident CTAs come from neighbouring block indices,
+// so two whole tiles could share an SM.) split_mode 3 (tests): stream-K
+// whatever it saves, a third of the tiles whole and the rest shared by 3/2
+// as many CTAs as tiles. Otherwise no stream-K.
+inline StreamK plan_stream_k(int64_t T, int slots, int sm_count, int nkt, int split_mode) {
+    StreamK s{(int)T, 0};
+    if (T <= 0 || nkt <= 0) return s;
+    if (split_mode == 3) {
+        const int64_t dp = T / 3, rest = T - dp;
+        const int64_t g = rest + (rest + 1) / 2;
+        s.dp_tiles = (int)dp;
+        s.sk_ctas = (int)(g < rest * nkt ? g : rest * nkt);  // no CTA without iterations
+        return s;
+    }
+    if (split_mode != 0 || sm_count <= 0 || slots < 2 * sm_count || nkt < 32) return s;
+    const int64_t P = sm_count;
+    if (T < P || T >= 2 * P || 10 * T > 18 * P) return s;
+    s.dp_tiles = 0;
+    s.sk_ctas = (int)(2 * P);
+    return s;
+}
+
 // Whether to give the FFMA kernel an MN-major copy of a K-major operand.
 // The kernel reads MN-major tiles with 16-byte copies (or TMA) and K-major
 // ones with transposing 4-byte copies (about 10% slower at 8192^3); a

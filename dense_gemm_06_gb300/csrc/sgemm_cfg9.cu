@@ -3,6 +3,7 @@
 // when both operands are MN-major with 16-byte aligned bases and row
 // pitches; other operand variants, and pitches the driver's tensor-map
 // encoder rejects, run configuration 7's cp.async kernel.
+#include "sgemm_sk.cuh"
 #include "sgemm_tma.cuh"
 
 namespace libgemm {
@@ -17,10 +18,13 @@ int launch_tma(SgemmParams sp, const CUtensorMap& ta, const CUtensorMap& tb,
                int fault_inject, cudaStream_t stream) {
     using Cfg = typename TC::Cfg;
     auto kern = sgemm_ffma_tma_kernel<TC>;
-    static std::atomic<uint64_t> configured{0};
+    auto kern_sk = sgemm_ffma_tma_sk_kernel<TC>;
+    static std::atomic<uint64_t> configured{0}, configured_sk{0};
     static std::atomic<int> per_sm[64];
     const int device = dev.device;
-    if (!configure_once(kern, configured, device, TC::SMEM)) return kCuda;
+    if (!configure_once(kern, configured, device, TC::SMEM) ||
+        !configure_once(kern_sk, configured_sk, device, TC::SMEM))
+        return kCuda;
     int occ = per_sm[device & 63].load();
     if (occ == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::THREADS, TC::SMEM) !=
@@ -30,26 +34,39 @@ int launch_tma(SgemmParams sp, const CUtensorMap& ta, const CUtensorMap& tb,
         }
         per_sm[device & 63].store(occ);
     }
-    plan_split(sp, occ > 0 ? occ * dev.sm_count : 0, dev.sm_count,
-               (sp.K + TC::BK - 1) / TC::BK, split_mode);
+    const int nkt = (sp.K + TC::BK - 1) / TC::BK;
+    SkArgs sk{0, nullptr};
+    plan_split(sp, occ > 0 ? occ * dev.sm_count : 0, dev.sm_count, nkt, split_mode, &sk.ctas);
     const int64_t tail = (int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles;
     if (tail > 0) {
-        const size_t bytes = (size_t)tail * sp.splits * BM * BN * sizeof(float);
-        sp.ws = scratch ? static_cast<float*>(scratch->get(bytes)) : nullptr;
+        // K-slices: a partial tile per slice; stream-K: one per stream-K CTA
+        // and the CTAs' flags
+        const size_t parts = sk.ctas > 0 ? (size_t)sk.ctas : (size_t)tail * sp.splits;
+        const size_t flags = sk.ctas > 0 ? (size_t)sk.ctas * 8 : 0;
+        sp.ws = scratch
+            ? static_cast<float*>(scratch->get(parts * BM * BN * sizeof(float) + flags))
+            : nullptr;
+        sk.flags = sp.ws && flags
+            ? reinterpret_cast<unsigned long long*>(sp.ws + parts * BM * BN)
+            : nullptr;
         if (!sp.ws) {  // no scratch: compute every tile whole
             sp.dp_tiles = sp.tiles_m * sp.tiles_n;
             sp.splits = 1;
+            sk.ctas = 0;
         }
     }
     const TmaArgs x{dev.err_word, next_generation(), (unsigned long long)wait_limit_ns,
                     fault_inject};
-    const int64_t units =
-        sp.dp_tiles + ((int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles) * sp.splits;
-    kern<<<dim3((unsigned)units), dim3(Cfg::THREADS), TC::SMEM, stream>>>(sp, ta, tb, x);
+    const int64_t fix = (int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles;
+    const int64_t units = sk.ctas > 0 ? sp.dp_tiles + sk.ctas : sp.dp_tiles + fix * sp.splits;
+    if (sk.ctas > 0)
+        kern_sk<<<dim3((unsigned)units), dim3(Cfg::THREADS), TC::SMEM, stream>>>(sp, ta, tb, x,
+                                                                                 sk);
+    else
+        kern<<<dim3((unsigned)units), dim3(Cfg::THREADS), TC::SMEM, stream>>>(sp, ta, tb, x);
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     note_launch();
-    const int64_t fix = (int64_t)sp.tiles_m * sp.tiles_n - sp.dp_tiles;
-    if (fix > 0) {
+    if (fix > 0 && sk.ctas == 0) {  // stream-K CTAs add up partials themselves
         sgemm_split_fixup_kernel<Cfg::TN>
             <<<dim3((unsigned)fix), dim3(Cfg::THREADS), 0, stream>>>(sp);
         if (cudaGetLastError() != cudaSuccess) return kCuda;

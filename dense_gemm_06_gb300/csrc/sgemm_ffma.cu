@@ -68,11 +68,24 @@ bool aligned16(const void* p, int64_t ld) {
 
 }  // namespace
 
-// Chooses the K-split of the tail tiles (the model is plan_tail_split's, in
-// policy.h).
-void plan_split(SgemmParams& sp, int slots, int sm_count, int nkt, int split_mode) {
-    const TailSplit t =
-        plan_tail_split((int64_t)sp.tiles_m * sp.tiles_n, slots, sm_count, nkt, split_mode);
+// Chooses the K-split of the tail tiles, or (kernels that support it) a
+// stream-K share of them (the models are plan_tail_split's and
+// plan_stream_k's, in policy.h).
+void plan_split(SgemmParams& sp, int slots, int sm_count, int nkt, int split_mode,
+                int* sk_ctas) {
+    const int64_t T = (int64_t)sp.tiles_m * sp.tiles_n;
+    if (sk_ctas) {
+        *sk_ctas = 0;
+        const StreamK s = plan_stream_k(T, slots, sm_count, nkt, split_mode);
+        if (s.sk_ctas > 0) {
+            sp.dp_tiles = s.dp_tiles;
+            sp.splits = 1;
+            sp.kt_slice = nkt;
+            *sk_ctas = s.sk_ctas;
+            return;
+        }
+    }
+    const TailSplit t = plan_tail_split(T, slots, sm_count, nkt, split_mode == 3 ? 1 : split_mode);
     sp.dp_tiles = t.dp_tiles;
     sp.splits = t.splits;
     sp.kt_slice = t.kt_slice;

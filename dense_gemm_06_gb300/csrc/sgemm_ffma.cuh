@@ -49,7 +49,11 @@ int launch_sgemm_cfg8(const SgemmParams& sp, int av, int bv, int device, int sm_
 
 // Chooses the K-split of the tail tiles (defined in sgemm_ffma.cu, with the
 // model it uses); fills sp.dp_tiles, sp.splits and sp.kt_slice.
-void plan_split(SgemmParams& sp, int slots, int sm_count, int nkt, int split_mode);
+// Plans the tail split (K-slices) of a launch; with sk_ctas non-null (the
+// TMA-fed kernel) it may instead plan stream-K and return its CTA count there
+// (0: none).
+void plan_split(SgemmParams& sp, int slots, int sm_count, int nkt, int split_mode,
+                int* sk_ctas = nullptr);
 
 namespace {
 

@@ -20,7 +20,8 @@
 //     k-tiles 7% slower, three CTAs per SM, which spills, 1.5% slower);
 //   * every wait is bounded (GEMM_OPT_WAIT_LIMIT_NS): one that runs out
 //     records a timeout in the device error word and the thread stops; thread
-//     0 then lets its copies in flight land (bounded) before the CTA exits.
+//     0 then lets its copies in flight land (bounded) before the CTA exits;
+//   * sgemm_sk.cuh holds its stream-K variant.
 #pragma once
 
 #include <cuda.h>

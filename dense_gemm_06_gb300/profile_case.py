@@ -29,6 +29,7 @@ CASES = {
     "sgemm": (8192, 8192, 8192, 0, 0, 0, "normal", 1027, 0, 0),
     "bf16": (8192, 8192, 8192, 4, 0, 0, "normal", 1028, 0, 0),
     "f16small": (1024, 512, 256, 1, 0, 0, "int", 1025, -5, 5),
+    "sgemm2048": (2048, 2048, 2048, 0, 1, 1, "pm1", 1026, 0, 0),
     "f16ragged": (4095, 3071, 1037, 1, 0, 1, "int", 1029, -3, 3),
     "f16skinny": (16384, 256, 8192, 1, 0, 1, "int", 1030, -3, 3),
     # 20 x 16 = 320 tiles of 128 x 128: a 16-tile last wave on 304 FFMA CTA slots

@@ -348,11 +348,15 @@ enum gemm_option {
        along K into 2-8 slices, computed by separate CTAs into pool scratch
        and summed in slice order by a fixup kernel before the epilogue, when
        a per-SM model predicts a saving of at least 10%, every slice keeps at
-       least 32 k-tiles, and there is no full round or at least two),
-       1 = never split, 2 = always split the last wave of resident CTAs into
-       2-4 slices (every tile when there is less than one wave; tests). A
-       split changes the order of the k-sum, never the per-product
-       rounding. */
+       least 32 k-tiles, and there is no full round or at least two; with
+       exactly one full round and at most 1.8 rounds' worth of tiles, the
+       TMA-fed kernel instead runs one whole tile per SM and shares the rest
+       of the tiles' k-iterations evenly over one more CTA per SM (stream-K),
+       whose partial tiles a fixup kernel adds in k order), 1 = never split,
+       2 = always split the last wave of resident CTAs into 2-4 slices (every
+       tile when there is less than one wave; tests), 3 = always stream-K in
+       the TMA-fed kernel (a third of the tiles whole; tests). A split changes
+       the order of the k-sum, never the per-product rounding. */
     GEMM_OPT_SIMT_SPLIT_TAIL = 9,
     /* Tile scheduler of the tensor-core kernel (the Gluon Multi-CTA
        tutorial's CLC-scheduled matmul): 0 = automatic (currently static),

@@ -7,6 +7,7 @@
 //   panel  M N K f32 ctas_per_sm cta_group multicast sm_count -> "rows"
 //   tcshape M N cta_group tile_n multicast sm_count         -> "cta_group tile_n"
 //   tcsplit T slots tile_n cta_group multicast mode          -> "split_from"
+//   sk T slots sm_count nkt mode                               -> "dp_tiles sk_ctas"
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -46,6 +47,12 @@ int main(int argc, char** argv) {
         std::printf("%lld\n", (long long)plan_tc_split(arg(argv, 2), arg(argv, 3),
                                                         (int)arg(argv, 4), (int)arg(argv, 5),
                                                         arg(argv, 6) != 0, (int)arg(argv, 7)));
+        return 0;
+    }
+    if (argc >= 7 && std::strcmp(argv[1], "sk") == 0) {
+        const StreamK k = plan_stream_k(arg(argv, 2), (int)arg(argv, 3), (int)arg(argv, 4),
+                                        (int)arg(argv, 5), (int)arg(argv, 6));
+        std::printf("%d %d\n", k.dp_tiles, k.sk_ctas);
         return 0;
     }
     std::fprintf(stderr, "usage: see the header of policy_probe.cc\n");

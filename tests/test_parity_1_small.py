@@ -160,6 +160,23 @@ def test_tc_split_last_round_of_many(cg, tile_n):
                       cta_group=cg, tile_n=tile_n, split=split)
 
 
+@pytest.mark.parametrize("shape", [(1000, 1001, 333), (300, 520, 2000), (2048, 2048, 256),
+                                   (129, 257, 17)])
+def test_sgemm_stream_k(shape):
+    # the TMA-fed FFMA kernel (MN-major operands, 16-byte rows) with stream-K
+    # forced: a third of the tiles whole, the others' k-iterations shared by
+    # 1.5x as many CTAs (ranges crossing tile boundaries, partial tiles summed
+    # in k order by the fixup kernel); integer data, so the sum is exact
+    M, N, K = shape
+    saved = lg.gemm_get_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL)
+    lg.check(lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 3))
+    try:
+        run_and_check(M, N, K, lg.GEMM_F32, 1, 1, 1, dist="int", seed=M + K)
+        run_and_check(M, N, K, lg.GEMM_F32, 1, 1, 0, dist="pm1", seed=K)
+    finally:
+        lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, saved)
+
+
 # ----------------------------------------------------- degenerate sizes --
 
 @pytest.mark.parametrize("dtype", [lg.GEMM_F32, lg.GEMM_BF16_F32, lg.GEMM_F16_F16])

@@ -147,3 +147,25 @@ def test_tc_split(probe):
     assert probe("tcsplit", 152, 76, 256, 2, 0, 2) == 76
     # occupancy unknown: never
     assert probe("tcsplit", 1024, 0, 256, 2, 0, 0) == 1024
+
+
+def test_stream_k(probe):
+    # fp32 2048^3: 256 tiles on 152 SMs (304 slots): every tile's iterations
+    # shared by 304 stream-K CTAs (two tiles' time -> 1.68)
+    assert probe("sk", 256, SLOTS, P, 128, 0) == (0, 304)
+    # 1.8 P (273.6) is the break-even of the 10% rule; 2 P or more: none
+    assert probe("sk", 273, SLOTS, P, 128, 0) == (0, 304)
+    assert probe("sk", 274, SLOTS, P, 128, 0) == (274, 0)
+    assert probe("sk", 304, SLOTS, P, 128, 0) == (304, 0)
+    # under one tile per SM (the K-slice rule's case), too few k-tiles, one
+    # CTA per SM only, or another mode: none
+    assert probe("sk", 151, SLOTS, P, 128, 0) == (151, 0)
+    assert probe("sk", 256, SLOTS, P, 31, 0) == (256, 0)
+    assert probe("sk", 256, P, P, 128, 0) == (256, 0)
+    assert probe("sk", 256, SLOTS, P, 128, 1) == (256, 0)
+    assert probe("sk", 256, SLOTS, P, 128, 2) == (256, 0)
+    # forced (tests): a third whole, the rest over 3/2 as many CTAs as tiles,
+    # never more CTAs than iterations
+    assert probe("sk", 30, SLOTS, P, 64, 3) == (10, 30)
+    assert probe("sk", 7, SLOTS, P, 64, 3) == (2, 8)
+    assert probe("sk", 4, SLOTS, P, 1, 3) == (1, 3)
