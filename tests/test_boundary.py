@@ -160,7 +160,8 @@ def test_strerror_and_options(lib):
     assert lg.gemm_get_option(lg.GEMM_OPT_SOFTMAX_FAULT_INJECT) == 0
     assert lg.gemm_set_option(lg.GEMM_OPT_SOFTMAX_FAULT_INJECT, 2) == lg.GEMM_ERR_INVALID_ARG
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL) == 0
-    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 3) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 4) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 3) == 0   # stream-K (tests)
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 2) == 0
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL) == 2
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_SPLIT_TAIL, 0) == 0
@@ -168,6 +169,16 @@ def test_strerror_and_options(lib):
     assert lg.gemm_set_option(lg.GEMM_OPT_TC_SCHEDULER, 3) == lg.GEMM_ERR_INVALID_ARG
     assert lg.gemm_get_option(lg.GEMM_OPT_SIMT_FAULT_INJECT) == 0
     assert lg.gemm_set_option(lg.GEMM_OPT_SIMT_FAULT_INJECT, 2) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_get_option(lg.GEMM_OPT_TC_TILE_N) == 0
+    for bad in (32, 96, 512, -1):
+        assert lg.gemm_set_option(lg.GEMM_OPT_TC_TILE_N, bad) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_set_option(lg.GEMM_OPT_TC_TILE_N, 64) == 0
+    assert lg.gemm_get_option(lg.GEMM_OPT_TC_TILE_N) == 64
+    assert lg.gemm_set_option(lg.GEMM_OPT_TC_TILE_N, 0) == 0
+    assert lg.gemm_get_option(lg.GEMM_OPT_TC_SPLIT_TAIL) == 0
+    assert lg.gemm_set_option(lg.GEMM_OPT_TC_SPLIT_TAIL, 3) == lg.GEMM_ERR_INVALID_ARG
+    assert lg.gemm_set_option(lg.GEMM_OPT_TC_SPLIT_TAIL, 2) == 0
+    assert lg.gemm_set_option(lg.GEMM_OPT_TC_SPLIT_TAIL, 0) == 0
 
 
 def test_launch_count_unchanged_by_rejected_calls(lib):
