@@ -4,6 +4,14 @@
     python -m dense_gemm_06_gb300.profile_case --case bf16 --n 8192 --reps 3
     python -m dense_gemm_06_gb300.profile_case --case f16skinny --reps 3
     python -m dense_gemm_06_gb300.profile_case --case f16small --reps 3
+    python -m dense_gemm_06_gb300.profile_case --case every
+
+--case every runs one small call of each kernel of the library (for a
+launch list that covers all of them): the tcgen05 GEMM at its small and
+ragged shapes (with the operand repack), the TMA-fed FFMA kernel with its
+K-slice tail and fixup, its stream-K variant, the cp.async FFMA kernel, the
+transpose pre-pass, the K = 0 kernels of gemm, gemm_ex and gemm_noalloc,
+gemm_noalloc's repack and the three row-softmax kernels.
 
 Inputs are the seeded synthetic operands of the benchmark (datagen), resident
 on the device before the first launch; each repetition is one gemm() call on
@@ -37,14 +45,79 @@ CASES = {
 }
 
 
+def run_every():
+    """One small call of every kernel of the library (see the module doc)."""
+    import torch
+
+    import datagen
+    import dense_gemm_06_gb300 as lg
+
+    torch.cuda.set_device(0)
+    lg.load()
+
+    def dev(M, K, major, it, dist, seed, stream, pad=0, lo=-3, hi=3):
+        ld = (K if major == 0 else M) + pad
+        a = datagen.operand(M, K, major=major, ld=ld, dtype=it, dist=dist, seed=seed,
+                            stream=stream, lo=lo, hi=hi)
+        return torch.from_numpy(a.view(np.int16) if it != "f32" else a).cuda(), ld
+
+    def run(what, M, N, K, dtype, am, bm, pad=0, opts=(), fn=None, ldc=None):
+        it, ot = lg.IN_TYPE[dtype], lg.OUT_TYPE[dtype]
+        dA, lda = dev(M, K, am, it, "int", 7, 0, pad)
+        dB, ldb = dev(N, K, bm, it, "int", 7, 1, pad)
+        ldc = ldc or N
+        dC = torch.zeros(M * ldc, dtype=torch.float32 if ot == "f32" else torch.int16,
+                         device="cuda")
+        saved = [(o, lg.gemm_get_option(o)) for o, _ in opts]
+        for o, v in opts:
+            lg.check(lg.gemm_set_option(o, v))
+        try:
+            lg.check((fn or lg.gemm)(M, N, K, dA, lda, am, dB, ldb, bm, dC, ldc, 1, dtype), what)
+            lg.check(lg.gemm_check_device_error(), what)
+        finally:
+            for o, v in saved:
+                lg.gemm_set_option(o, v)
+        print(f"every: {what}", flush=True)
+
+    run("tcgen05, 1024x512x256 bf16 (one CTA per 128x64 tile)", 1024, 512, 256,
+        lg.GEMM_BF16_F32, 0, 0)
+    run("tcgen05 + repack, 1000x777x1037 fp16, misaligned A, B, C", 1000, 777, 1037,
+        lg.GEMM_F16_F32, 0, 1, pad=1, ldc=779)
+    run("FFMA TMA-fed + K-slice fixup, 1024x1024x8192", 1024, 1024, 8192, lg.GEMM_F32, 1, 1)
+    run("FFMA TMA-fed stream-K, 2048^3", 2048, 2048, 2048, lg.GEMM_F32, 1, 1)
+    run("FFMA cp.async (configuration 7), 300x520x200 K-major", 300, 520, 200, lg.GEMM_F32, 0,
+        0, opts=((lg.GEMM_OPT_SIMT_CONFIG, 7),))
+    run("transpose pre-pass + FFMA, 1024^3 K-major", 1024, 1024, 1024, lg.GEMM_F32, 0, 0,
+        opts=((lg.GEMM_OPT_SIMT_TRANSPOSE, 2),))
+    run("K = 0 (zero fill)", 300, 500, 0, lg.GEMM_F32, 0, 0)
+    run("gemm_noalloc + its repack, 1000x777x1037 fp16 misaligned", 1000, 777, 1037,
+        lg.GEMM_F16_F32, 0, 1, pad=1, fn=lg.gemm_noalloc)
+    run("gemm_noalloc K = 0", 300, 500, 0, lg.GEMM_F16_F32, 0, 0, fn=lg.gemm_noalloc)
+    C = torch.ones(300 * 500, dtype=torch.float32, device="cuda")
+    lg.check(lg.gemm_ex(300, 500, 0, 0, 1, 0, 0, 1, 0, C, 500, 1, lg.GEMM_F32, beta=0.5),
+             "gemm_ex K = 0")
+    print("every: gemm_ex K = 0 (epilogue only)", flush=True)
+    for M, N in ((4096, 512), (4096, 8192), (256, 65536), (256, 65537)):
+        x = torch.randn(M * N, dtype=torch.float32, device="cuda")
+        y = torch.empty_like(x)
+        lg.check(lg.softmax_rows(M, N, x, N, y, N), "softmax_rows")
+        print(f"every: softmax_rows {M} x {N}", flush=True)
+    lg.check(lg.gemm_check_device_error(), "device error word")
+
+
 def main(argv=None):
     import torch
 
     import datagen
     import dense_gemm_06_gb300 as lg
 
+    if argv is None:
+        argv = sys.argv[1:]
+    if "--case" in argv and argv[argv.index("--case") + 1:argv.index("--case") + 2] == ["every"]:
+        run_every()
+        return
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=sorted(CASES), required=True)
+    ap.add_argument("--case", choices=sorted(CASES) + ["every"], required=True)
     ap.add_argument("--n", type=int, default=None, help="override M = N = K")
     ap.add_argument("--shape", type=int, nargs=3, metavar=("M", "N", "K"), default=None,
                     help="override M, N and K")
