@@ -590,13 +590,15 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         if ((pd.M + rows - 1) / rows > kMaxPanels) rows = pd.M;
         const int np = (int)((pd.M + rows - 1) / rows);
 
-        // Events: allocation done (s), B (and A unless it goes by panels)
-        // in, each A panel in, each C panel computed, both copy streams done.
-        cudaEvent_t ev[2 * kMaxPanels + 4] = {};
+        // Events: allocation done (s), each input piece in (B and the first
+        // A panel in up to 4 pieces, the other A panels), each C panel
+        // computed, both copy streams done.
+        constexpr int kMaxEvents = 2 * kMaxPanels + 8;
+        cudaEvent_t ev[kMaxEvents] = {};
         int nev = 0;
         auto event = [&]() -> cudaEvent_t {
             cudaEvent_t e = nullptr;
-            if (nev < 2 * kMaxPanels + 4 &&
+            if (nev < kMaxEvents &&
                 cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess) {
                 ev[nev++] = e;
                 return e;
@@ -608,69 +610,93 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
             if (e != cudaSuccess && rc == kOk) rc = kCuda;
             return rc == kOk;
         };
-        // A panel of A's rows is one copy of contiguous rows when A (in the
-        // normalised problem) is K-major; otherwise A goes in whole with B.
-        const bool a_panels = np > 1;  // A goes in panel by panel (either major)
+        // A goes in panel by panel (either major) when there are several.
+        const bool a_panels = np > 1;
         const int64_t prow = rows;
-        Problem pb = pd;             // B replaced by its MN-major copy, if made
+        // With an fp32 C the first panel is pipelined over K as well: B and
+        // that panel's A arrive in kp pieces of K, and the panel runs as kp
+        // GEMMs, each adding its product to C (fused epilogue, beta = 1), so
+        // its first GEMM starts once a kp-th of B is in instead of all of it.
+        // (A 16-bit C would be rounded between the pieces, so it goes whole.)
+        constexpr int kKp = 4;
+        const int kp = (np > 1 && oe == 4 && K >= kKp * 256) ? kKp : 1;
+        auto kbound = [&](int j) { return j == kp ? K : round_up(K * j / kp, 64); };
+        Problem pb = pd;  // B replaced by its MN-major copy, if made
         void* bt = nullptr;
-        cudaEvent_t e_alloc = event(), e_b = event();
-        if (!e_alloc || !e_b) rc = kCuda;
-        if (rc == kOk && ok(cudaEventRecord(e_alloc, s)) &&
-            ok(cudaStreamWaitEvent(h2d, e_alloc, 0)) && K > 0) {
-            const char* hB = static_cast<const char*>(ph.B);
-            char* dBp = static_cast<char*>(const_cast<void*>(pd.B));
-            const int64_t bi = pd.b_kmajor ? K : pd.N, bo = pd.b_kmajor ? pd.N : K;
-            ok(copy(dBp, pd.ldb * ie, hB, ph.ldb * ie, bi * ie, bo, cudaMemcpyHostToDevice, h2d));
-            if (!a_panels) {  // one panel: all of A with B
-                const int64_t ai = pd.a_kmajor ? K : pd.M, ao = pd.a_kmajor ? pd.M : K;
-                ok(copy(const_cast<void*>(pd.A), pd.lda * ie, ph.A, ph.lda * ie, ai * ie, ao,
-                        cudaMemcpyHostToDevice, h2d));
-            }
-        }
-        if (rc == kOk) ok(cudaEventRecord(e_b, h2d));
-        if (rc == kOk) ok(cudaStreamWaitEvent(s, e_b, 0));
+        cudaEvent_t e_alloc = event();
+        if (!e_alloc) rc = kCuda;
+        if (rc == kOk) ok(cudaEventRecord(e_alloc, s));
+        if (rc == kOk) ok(cudaStreamWaitEvent(h2d, e_alloc, 0));
         // A K-major fp32 B that every panel would transpose for the FFMA
-        // kernel is transposed once here instead.
+        // kernel is transposed once instead (piece by piece as it arrives).
+        bool b_transpose = false;
         if (rc == kOk && np > 1 && K > 0 && dtype == GEMM_F32 && pd.b_kmajor) {
-            Problem q0 = pd;
-            q0.M = prow;
-            if (want_transpose(q0.M, q0.M, q0.N, q0.K, cfg.simt_transpose)) {
+            if (want_transpose(prow, prow, pd.N, K, cfg.simt_transpose)) {
                 const int64_t ld2 = round_up(pd.N, 4);
                 if (cudaMallocFromPoolAsync(&bt, (size_t)(K * ld2 * 4), pool, s) != cudaSuccess) {
                     cudaGetLastError();
                     bt = nullptr;
                     rc = kCuda;
                 } else {
-                    rc = launch_transpose_f32(static_cast<const float*>(pd.B), pd.ldb,
-                                              static_cast<float*>(bt), ld2, pd.N, K, *dev, s);
                     pb.B = bt;
                     pb.ldb = ld2;
                     pb.b_kmajor = false;
+                    b_transpose = true;
                 }
             }
         }
+        // Copies of B's k-range [k0, k1) and of rows m0 .. m1 of A's k-range.
+        auto copy_b = [&](int64_t k0, int64_t k1) {
+            const char* hB = static_cast<const char*>(ph.B);
+            char* dBp = static_cast<char*>(const_cast<void*>(pd.B));
+            if (pd.b_kmajor)  // columns k0 .. k1 of every row of B
+                return ok(copy(dBp + k0 * ie, pd.ldb * ie, hB + k0 * ie, ph.ldb * ie,
+                               (k1 - k0) * ie, pd.N, cudaMemcpyHostToDevice, h2d));
+            return ok(copy(dBp + k0 * pd.ldb * ie, pd.ldb * ie, hB + k0 * ph.ldb * ie,
+                           ph.ldb * ie, pd.N * ie, k1 - k0, cudaMemcpyHostToDevice, h2d));
+        };
+        auto copy_a = [&](int64_t m0, int64_t m1, int64_t k0, int64_t k1) {
+            const char* hA = static_cast<const char*>(ph.A);
+            char* dAp = static_cast<char*>(const_cast<void*>(pd.A));
+            if (pd.a_kmajor)  // rows m0 .. m1, columns k0 .. k1
+                return ok(copy(dAp + (m0 * pd.lda + k0) * ie, pd.lda * ie,
+                               hA + (m0 * ph.lda + k0) * ie, ph.lda * ie, (k1 - k0) * ie, m1 - m0,
+                               cudaMemcpyHostToDevice, h2d));
+            return ok(copy(dAp + (k0 * pd.lda + m0) * ie, pd.lda * ie, hA + (k0 * ph.lda + m0) * ie,
+                           ph.lda * ie, (m1 - m0) * ie, k1 - k0, cudaMemcpyHostToDevice, h2d));
+        };
         for (int i = 0; i < np && rc == kOk; ++i) {
             const int64_t m0 = i * prow, m1 = std::min<int64_t>(pd.M, m0 + prow);
             Problem q = pb;
             q.M = m1 - m0;
             q.C = static_cast<char*>(pd.C) + m0 * pd.ldc * oe;
             if (K > 0) q.A = static_cast<const char*>(pd.A) + (pd.a_kmajor ? m0 * pd.lda : m0) * ie;
-            if (a_panels && K > 0) {
-                cudaEvent_t e_a = event();
-                if (!e_a) { rc = kCuda; break; }
-                if (pd.a_kmajor)  // rows m0 .. m1 of A
-                    ok(copy(const_cast<void*>(q.A), pd.lda * ie,
-                            static_cast<const char*>(ph.A) + m0 * ph.lda * ie, ph.lda * ie,
-                            K * ie, q.M, cudaMemcpyHostToDevice, h2d));
-                else              // columns m0 .. m1 of every k-row of A
-                    ok(copy(const_cast<void*>(q.A), pd.lda * ie,
-                            static_cast<const char*>(ph.A) + m0 * ie, ph.lda * ie, q.M * ie, K,
-                            cudaMemcpyHostToDevice, h2d));
-                if (rc == kOk) ok(cudaEventRecord(e_a, h2d));
-                if (rc == kOk) ok(cudaStreamWaitEvent(s, e_a, 0));
+            // panel 0 in kp pieces of K (B piece by piece with it); later
+            // panels whole, once their A rows are in (B is in by then)
+            const int pieces = i == 0 ? kp : 1;
+            for (int j = 0; j < pieces && rc == kOk; ++j) {
+                const int64_t k0 = i == 0 ? kbound(j) : 0, k1 = i == 0 ? kbound(j + 1) : K;
+                if (K > 0) {
+                    cudaEvent_t e_in = event();
+                    if (!e_in) { rc = kCuda; break; }
+                    if (i == 0) copy_b(k0, k1);
+                    if (rc == kOk && (a_panels || i == 0)) copy_a(m0, m1, k0, k1);
+                    if (rc == kOk) ok(cudaEventRecord(e_in, h2d));
+                    if (rc == kOk) ok(cudaStreamWaitEvent(s, e_in, 0));
+                }
+                if (rc == kOk && i == 0 && b_transpose)
+                    rc = launch_transpose_f32(static_cast<const float*>(pd.B) + k0, pd.ldb,
+                                              static_cast<float*>(bt) + k0 * pb.ldb, pb.ldb,
+                                              pd.N, k1 - k0, *dev, s);
+                Problem qk = q;
+                if (pieces > 1) {
+                    qk.K = k1 - k0;
+                    qk.A = static_cast<const char*>(q.A) + (pb.a_kmajor ? k0 : k0 * pb.lda) * ie;
+                    qk.B = static_cast<const char*>(q.B) + (pb.b_kmajor ? k0 : k0 * pb.ldb) * ie;
+                    if (j > 0) qk.epi = EpiParams{1, 1.f, 1.f, nullptr, 0, GEMM_ACT_NONE};
+                }
+                if (rc == kOk) rc = run_device(qk, *dev, pool, cfg, s);
             }
-            if (rc == kOk) rc = run_device(q, *dev, pool, cfg, s);
             cudaEvent_t e_c = rc == kOk ? event() : nullptr;
             if (rc == kOk && !e_c) rc = kCuda;
             if (rc == kOk) ok(cudaEventRecord(e_c, s));
