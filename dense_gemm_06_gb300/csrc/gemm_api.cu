@@ -11,6 +11,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -273,6 +276,8 @@ int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCon
         }
         rc = launch_transpose_f32(static_cast<const float*>(*ops[i]), *lds[i],
                                   static_cast<float*>(scratch[i]), ld2, rows[i], p.K, dev, s);
+        dispatch_log("transpose of K-major fp32 %s (%lld x %lld) to MN-major", i ? "B" : "A",
+                     (long long)rows[i], (long long)p.K);
         *ops[i] = scratch[i];
         *lds[i] = ld2;
         *kmaj[i] = false;
@@ -329,6 +334,8 @@ int run_device(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunCo
                           s>>>(job[0], job[1]);
         if (cudaGetLastError() != cudaSuccess) rc = kCuda;
         else note_launch();
+        dispatch_log("repack of misaligned 16-bit operands: A %s, B %s (%lld bytes of scratch)",
+                     job[0].outer ? "yes" : "no", job[1].outer ? "yes" : "no", (long long)bytes);
     }
     if (rc == kOk) {
         TcLaunch o = tc_launch(cfg);
@@ -386,6 +393,24 @@ TcLaunch tc_launch(const RunConfig& c) {
 }  // namespace
 
 void note_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+bool dispatch_log_on() {
+    static const bool on = [] {
+        const char* v = std::getenv("GEMM_LOG");
+        return v && v[0] && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+void dispatch_log(const char* fmt, ...) {
+    if (!dispatch_log_on()) return;
+    char line[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(line, sizeof(line), fmt, ap);
+    va_end(ap);
+    std::fprintf(stderr, "libgemm: %s\n", line);
+}
 
 namespace {
 
@@ -621,6 +646,9 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         constexpr int kKp = 4;
         const int kp = (np > 1 && oe == 4 && K >= kKp * 256) ? kKp : 1;
         auto kbound = [&](int j) { return j == kp ? K : round_up(K * j / kp, 64); };
+        dispatch_log("gemm_host %lldx%lldx%lld: %d row panel(s) of %lld rows, the first in %d "
+                     "piece(s) of K",
+                     (long long)pd.M, (long long)pd.N, (long long)K, np, (long long)rows, kp);
         Problem pb = pd;  // B replaced by its MN-major copy, if made
         void* bt = nullptr;
         cudaEvent_t e_alloc = event();

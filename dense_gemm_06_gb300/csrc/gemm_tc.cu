@@ -243,13 +243,28 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, const TcLaunch& o,
     if ((int64_t)tp.tiles_m * tp.tiles_n * 2 * CG > 0x7fffffffLL) return kUnsupported;
 
     const bool a_mn = !pr.a_kmajor, b_mn = !pr.b_kmajor;
+    int rc = kInvalidArg;
     switch (pr.dtype) {
-        case 1: return launch_gemm_tc_f16_f32(tp, CG, mc, a_mn, b_mn, dev, stream);
-        case 2: return launch_gemm_tc_bf16_f32(tp, CG, mc, a_mn, b_mn, dev, stream);
-        case 3: return launch_gemm_tc_f16_f16(tp, CG, mc, a_mn, b_mn, dev, stream);
-        case 4: return launch_gemm_tc_bf16_bf16(tp, CG, mc, a_mn, b_mn, dev, stream);
-        default: return kInvalidArg;
+        case 1: rc = launch_gemm_tc_f16_f32(tp, CG, mc, a_mn, b_mn, dev, stream); break;
+        case 2: rc = launch_gemm_tc_bf16_f32(tp, CG, mc, a_mn, b_mn, dev, stream); break;
+        case 3: rc = launch_gemm_tc_f16_f16(tp, CG, mc, a_mn, b_mn, dev, stream); break;
+        case 4: rc = launch_gemm_tc_bf16_bf16(tp, CG, mc, a_mn, b_mn, dev, stream); break;
+        default: break;
     }
+    if (rc == kOk && dispatch_log_on()) {
+        // launch_variant has planned the split (tp.split_from) by now
+        const int rows_u = mc ? (tp.tiles_m + 1) / 2 : tp.tiles_m;
+        const int tiles = rows_u * tp.tiles_n;
+        dispatch_log("tcgen05 %dx%dx%d: %s, %d x %d tiles (%d x %d), %d work units (tiles from "
+                     "%d run as two half-width units), %s schedule, A %s, B %s, C by %s%s%s",
+                     tp.M, tp.N, tp.K, CG == 2 ? "CTA pairs" : "one CTA per tile", tile_m,
+                     tp.tile_n, tp.tiles_m, tp.tiles_n, tp.split_from + 2 * (tiles - tp.split_from),
+                     tp.split_from, tp.clc ? "cluster-launch-control" : "persistent static",
+                     a_mn ? "MN-major" : "K-major", b_mn ? "MN-major" : "K-major",
+                     tp.c_tma ? "TMA stores" : "st.global", mc ? ", B multicast over two pairs" : "",
+                     tp.pdl ? ", waits on the repack (programmatic launch)" : "");
+    }
+    return rc;
 }
 
 }  // namespace libgemm

@@ -117,6 +117,17 @@ int launch_gemm_tc(const Problem& p, const DeviceInfo& dev, const TcLaunch& o,
 
 void note_launch(uint64_t n = 1);
 
+// Dispatch log (debug aid): when the environment variable GEMM_LOG is set to
+// a non-empty value other than "0" when the library first checks it, every
+// call writes one line per decision it takes (kernel, tile shape, split,
+// repack, transpose) to stderr, prefixed "libgemm: ". Off by default.
+bool dispatch_log_on();
+void dispatch_log(const char* fmt, ...)
+#if defined(__GNUC__)
+    __attribute__((format(printf, 1, 2)))
+#endif
+    ;
+
 // Host-side argument checks and layout normalisation of gemm() (no CUDA calls),
 // and the current device's error-word address (cudaGetSymbolAddress only).
 int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_major,

@@ -66,6 +66,15 @@ int launch_tma(SgemmParams sp, const CUtensorMap& ta, const CUtensorMap& tb,
         kern<<<dim3((unsigned)units), dim3(Cfg::THREADS), TC::SMEM, stream>>>(sp, ta, tb, x);
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     note_launch();
+    if (sk.ctas > 0)
+        dispatch_log("FFMA SGEMM (TMA) %dx%dx%d: %d x %d tiles of 128 x 128, %d whole, "
+                     "%d stream-K CTAs over the rest",
+                     sp.M, sp.N, sp.K, sp.tiles_m, sp.tiles_n, sp.dp_tiles, sk.ctas);
+    else
+        dispatch_log("FFMA SGEMM (TMA) %dx%dx%d: %d x %d tiles of 128 x 128, %d whole, "
+                     "the rest in %d K-slices of %d k-tiles",
+                     sp.M, sp.N, sp.K, sp.tiles_m, sp.tiles_n, sp.dp_tiles, sp.splits,
+                     sp.kt_slice);
     if (fix > 0 && sk.ctas == 0) {  // stream-K CTAs add up partials themselves
         sgemm_split_fixup_kernel<Cfg::TN>
             <<<dim3((unsigned)fix), dim3(Cfg::THREADS), 0, stream>>>(sp);

@@ -137,6 +137,12 @@ int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, int s
     const int av = pr.a_kmajor ? 0 : (aligned16(pr.A, pr.lda) ? 4 : 1);
     const int bv = pr.b_kmajor ? 0 : (aligned16(pr.B, pr.ldb) ? 4 : 1);
     const int d = dev.device, n = dev.sm_count;
+    if (config != 9)
+        dispatch_log("FFMA SGEMM (cp.async) %dx%dx%d: configuration %d, %d x %d tiles of 128 x 128, "
+                     "A %s, B %s",
+                     sp.M, sp.N, sp.K, config < 1 || config > 8 ? 1 : config, sp.tiles_m,
+                     sp.tiles_n, av == 0 ? "K-major" : "MN-major",
+                     bv == 0 ? "K-major" : "MN-major");
     switch (config) {
         case 2: return launch_sgemm_cfg2(sp, av, bv, d, n, split_mode, scratch, stream);
         case 3: return launch_sgemm_cfg3(sp, av, bv, d, n, split_mode, scratch, stream);
