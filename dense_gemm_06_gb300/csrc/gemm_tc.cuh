@@ -153,6 +153,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Tc
     return wait_slow(bar, parity, p.err, p.gen, p.wait_limit_ns);
 }
 
+// One lane of the (converged) warp: the issuing lane of the producer and MMA
+// roles, whose loops the whole warp runs so that their state stays
+// warp-uniform (TMA and MMA operands are taken from uniform registers).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
+
+// Bounded wait taken by every lane of a warp; the outcome is warp-uniform.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const TcParams& p) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, p));
+}
+
 // Spin (bounded by time, no barrier) to let in-flight async copies land.
 __device__ __noinline__ void grace_period_ns(uint64_t ns) {
     const uint64_t t0 = globaltimer_ns();
@@ -492,7 +510,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
-        if (lane == 0) {
+        // The warp runs the loop; one elected lane issues the copies.
+        {
             pdl_wait();  // operands written by the kernel before this one (repack)
             int stage = 0;
             uint32_t phase = 0;
@@ -505,13 +524,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 // bytes both CTAs of the pair load per stage (OOB fill included)
                 const uint32_t bytes = (uint32_t)(CG * (C_::A_BYTES + b_rows * BK * 2));
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(empty_bar(stage), phase ^ 1u, p)) { aborted = true; break; }
+                    if (!wait_bar_warp(empty_bar(stage), phase ^ 1u, p)) { aborted = true; break; }
                     const uint32_t fb =
                         CG == 2 ? mapa_shared(full_bar(stage), lead) : full_bar(stage);
-                    if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes);
                     const uint32_t sa = sA0 + stage * C_::A_BYTES;
                     const uint32_t sb = sB0 + stage * C_::B_BYTES;
                     const int k0 = kb * BK;
+                    if (elect_one()) {
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes);
                     if (kb == 0 && t == cluster) TC_TRACE(p, 2);
                     if constexpr (!A_MN) {
                         tma_load_2d<CG>(sa, &p.tmap_a, fb, k0, a_row);
@@ -539,16 +559,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                             tma_load_2d<CG>(sb + j * 64 * BK * 2, &p.tmap_b, fb,
                                             b_row + 64 * j, k0);
                     }
+                    }
+                    __syncwarp();
                     if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
                 }
-                if (aborted || !advance(t, j, false)) { aborted = true; break; }
+                if (aborted || !advance(t, j, true)) { aborted = true; break; }
             }
             if (aborted) grace_period_ns(200000);  // let issued copies land
         }
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
-        if (leader && lane == 0) {
+        // The leader's warp runs the loop; one elected lane issues the MMAs
+        // and the commits.
+        if (leader) {
             // instruction descriptor without N (bits 17-22 = N >> 3, per unit)
             constexpr uint32_t idesc0 =
                 make_idesc_f16(BF16, A_MN, B_MN, (uint32_t)C_::TILE_M, 0u);
@@ -558,45 +582,59 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             uint32_t acc_phase = 0;
             int j = 0;
             int nt = 0;  // units issued (trace slots)
+            // Shared-memory descriptors of stage 0 (128-byte swizzle) and the
+            // step between the 16-deep k-slices of one MMA each: K-major
+            // +32 bytes inside the swizzled 128-byte rows, MN-major +16
+            // k-rows of 128 bytes (two 8-row atoms).
+            const uint64_t a_desc0 = A_MN ? make_sdesc_sw128(sA0, 64 * BK * 2, 1024)
+                                          : make_sdesc_sw128(sA0, 16, 1024);
+            const uint64_t b_desc0 = B_MN ? make_sdesc_sw128(sB0, 64 * BK * 2, 1024)
+                                          : make_sdesc_sw128(sB0, 16, 1024);
+            constexpr int A_STEP = A_MN ? UMMA_K * 128 : UMMA_K * 2;
+            constexpr int B_STEP = B_MN ? UMMA_K * 128 : UMMA_K * 2;
             for (int t = cluster; t < total_units && !aborted;) {
                 const uint32_t idesc = idesc0 | ((uint32_t)(unit_of(t).width >> 3) << 17);
-                if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, p)) { aborted = true; break; }
+                if (!wait_bar_warp(acce_bar(acc), acc_phase ^ 1u, p)) { aborted = true; break; }
                 tc_fence_after_sync();
-                TC_TRACE(p, 4 + 4 * nt);
+                if (lane == 0) TC_TRACE(p, 4 + 4 * nt);
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(full_bar(stage), phase, p)) { aborted = true; break; }
+                    if (!wait_bar_warp(full_bar(stage), phase, p)) { aborted = true; break; }
                     tc_fence_after_sync();
-                    if (kb == 0 && nt == 0) TC_TRACE(p, 3);
-                    const uint32_t sa = sA0 + stage * C_::A_BYTES;
-                    const uint32_t sb = sB0 + stage * C_::B_BYTES;
+                    if (kb == 0 && nt == 0 && lane == 0) TC_TRACE(p, 3);
+                    // the stage's descriptors: the ring's first ones plus the
+                    // stage offset (the address field counts 16-byte units)
+                    const uint64_t ad = a_desc0 + (uint64_t)(stage * (C_::A_BYTES >> 4));
+                    const uint64_t bd = b_desc0 + (uint64_t)(stage * (C_::B_BYTES >> 4));
+                    if (elect_one()) {
 #pragma unroll
-                    for (int j = 0; j < BK / UMMA_K; ++j) {
-                        // K-major: +32 bytes inside the swizzled 128-byte row;
-                        // MN-major: +16 k-rows of 128 bytes (two 8-row atoms).
-                        const uint64_t ad = A_MN
-                            ? make_sdesc_sw128(sa + j * UMMA_K * 128, 64 * BK * 2, 1024)
-                            : make_sdesc_sw128(sa + j * UMMA_K * 2, 16, 1024);
-                        const uint64_t bd = B_MN
-                            ? make_sdesc_sw128(sb + j * UMMA_K * 128, 64 * BK * 2, 1024)
-                            : make_sdesc_sw128(sb + j * UMMA_K * 2, 16, 1024);
-                        mma_f16<CG>(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
-                    }
+                    for (int j = 0; j < BK / UMMA_K; ++j)
+                        mma_f16<CG>(d_tmem, ad + (uint64_t)(j * (A_STEP >> 4)),
+                                    bd + (uint64_t)(j * (B_STEP >> 4)), idesc,
+                                    (kb | j) != 0 ? 1u : 0u);
                     if constexpr (MC) mma_commit_pair(empty_bar(stage), (uint16_t)0xF);
                     else mma_commit<CG>(empty_bar(stage));
+                    }
+                    __syncwarp();
                     if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (aborted) break;
-                if constexpr (MC) mma_commit_pair(accf_bar(acc), (uint16_t)(0x3u << (2 * pair)));
-                else mma_commit<CG>(accf_bar(acc));
-                TC_TRACE(p, 5 + 4 * nt);
+                if (elect_one()) {
+                    if constexpr (MC) mma_commit_pair(accf_bar(acc), (uint16_t)(0x3u << (2 * pair)));
+                    else mma_commit<CG>(accf_bar(acc));
+                }
+                __syncwarp();
+                if (lane == 0) TC_TRACE(p, 5 + 4 * nt);
                 ++nt;
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-                if (!advance(t, j, false)) { aborted = true; break; }
+                if (!advance(t, j, true)) { aborted = true; break; }
             }
             // Drain: wait (bounded) until every MMA issued above has completed.
-            if constexpr (CG == 2) mma_commit_pair(drain_bar, (uint16_t)(1u << crank));
-            else mma_commit_local(drain_bar);
+            if (elect_one()) {
+                if constexpr (CG == 2) mma_commit_pair(drain_bar, (uint16_t)(1u << crank));
+                else mma_commit_local(drain_bar);
+            }
+            __syncwarp();
             uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < 1000000000ull) {
             }
