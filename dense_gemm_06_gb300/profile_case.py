@@ -5,6 +5,7 @@
     python -m dense_gemm_06_gb300.profile_case --case f16skinny --reps 3
     python -m dense_gemm_06_gb300.profile_case --case f16small --reps 3
     python -m dense_gemm_06_gb300.profile_case --case every
+    python -m dense_gemm_06_gb300.profile_case --case bf16 --vendor --reps 2
 
 --case every runs one small call of each kernel of the library (for a
 launch list that covers all of them): the tcgen05 GEMM at its small and
@@ -18,6 +19,11 @@ on the device before the first launch; each repetition is one gemm() call on
 one stream, so a profiler sees exactly `reps` launches of the kernel (plus a
 repack launch per misaligned operand for the ragged case). Prints the
 CUDA-event time of every repetition (not a benchmark number).
+
+--vendor runs torch.matmul (cuBLAS) on the same device operands instead of
+the library, for a side-by-side capture of the vendor kernel (16-bit inputs
+and C, both operands K-major). It is a comparison point for profiles,
+never a path of the library.
 """
 
 from __future__ import annotations
@@ -131,6 +137,8 @@ def main(argv=None):
     ap.add_argument("--simt-split", type=int, default=0,
                     help="FFMA last-wave K-split: 1 never, 2 always (0: automatic)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--vendor", action="store_true",
+                    help="run torch.matmul (cuBLAS) on the same operands instead")
     ap.add_argument("--tune", action="store_true",
                     help="run gemm_tune first (records the fastest configuration)")
     a = ap.parse_args(argv)
@@ -166,10 +174,21 @@ def main(argv=None):
                              s.cuda_stream)
         lg.check(rc, "gemm_tune")
         print(f"{a.case} {M}x{N}x{K} A{'KM'[am]} B{'KN'[bm]} tuned: {t}")
+    if a.vendor:
+        if it == "f32" or ot == "f32" or am != 0 or bm != 0:
+            raise SystemExit("--vendor: 16-bit inputs and C, both operands K-major")
+        tt = torch.bfloat16 if it == "bf16" else torch.float16
+        tA, tB = dA.view(tt).view(M, K), dB.view(tt).view(N, K)
+        tC = dC.view(tt).view(M, N)
     for r in range(a.reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        lg.check(lg.gemm(M, N, K, dA, lda, am, dB, ldb, bm, dC, N, 1, dtype, s.cuda_stream))
+        if a.vendor:
+            with torch.cuda.stream(s):
+                torch.matmul(tA, tB.t(), out=tC)
+        else:
+            lg.check(lg.gemm(M, N, K, dA, lda, am, dB, ldb, bm, dC, N, 1, dtype,
+                             s.cuda_stream))
         e1.record(s)
         s.synchronize()
         ms = e0.elapsed_time(e1)
