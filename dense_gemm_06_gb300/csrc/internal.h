@@ -66,17 +66,20 @@ __device__ __forceinline__ void gen_record_timeout(ErrWord* err, ErrWord gen) {
 // report through note_launch().
 // Stream-ordered scratch for one launch sequence: get() allocates once from
 // the pool; the caller frees `ptr` on the stream after the launches.
+// Device scratch of one call, enqueued on `stream`: get() returns the
+// buffer (its first call sizes it), release() ends the call's use of it.
+// Buffers up to 64 MB come from a per-(device, stream) cache that keeps them
+// across calls (see scratch_cache_acquire in gemm_api.cu); larger ones, and
+// any the cache cannot give, are stream-ordered pool allocations freed on
+// release.
 struct Scratch {
     cudaMemPool_t pool;
     cudaStream_t stream;
+    int device;
     void* ptr = nullptr;
-    void* get(size_t bytes) {
-        if (!ptr && cudaMallocFromPoolAsync(&ptr, bytes, pool, stream) != cudaSuccess) {
-            cudaGetLastError();
-            ptr = nullptr;
-        }
-        return ptr;
-    }
+    int slot = -1;  // >= 0: the cache entry lent to this call
+    void* get(size_t bytes);
+    void release();
 };
 // config: the FFMA tile configuration, 1..9 (GEMM_OPT_SIMT_CONFIG in gemm.h).
 // split_mode: 0 automatic (K-split the tiles after the last full round of
