@@ -277,6 +277,7 @@ struct CachedScratch {
     void* ptr = nullptr;
     size_t bytes = 0;
     cudaEvent_t last_use = nullptr;  // recorded on the entry's stream at each release
+    bool recorded = false;           // last_use covers every use so far (else never evicted)
     bool busy = false;
     uint64_t tick = 0;               // last release, for least-recently-used eviction
 };
@@ -314,11 +315,11 @@ int scratch_cache_acquire(int device, cudaStream_t s, size_t bytes, cudaMemPool_
             if (!g_scratch[i].ptr && !g_scratch[i].busy) slot = i;
         for (int i = 0; i < kCachedScratchEntries && slot < 0; ++i) {
             const CachedScratch& e = g_scratch[i];
-            if (e.busy || e.device != device) continue;
+            if (e.busy || !e.recorded || e.device != device) continue;
             int lru = i;
             for (int k = i + 1; k < kCachedScratchEntries; ++k)
-                if (!g_scratch[k].busy && g_scratch[k].device == device &&
-                    g_scratch[k].tick < g_scratch[lru].tick)
+                if (!g_scratch[k].busy && g_scratch[k].recorded &&
+                    g_scratch[k].device == device && g_scratch[k].tick < g_scratch[lru].tick)
                     lru = k;
             slot = lru;
         }
@@ -345,6 +346,7 @@ int scratch_cache_acquire(int device, cudaStream_t s, size_t bytes, cudaMemPool_
         }
         e.device = device;
         e.stream_id = id;
+        e.recorded = false;
     }
     CachedScratch& e = g_scratch[slot];
     if (e.bytes < bytes) {  // grow: earlier uses were on this stream, so ordered
@@ -365,7 +367,12 @@ int scratch_cache_acquire(int device, cudaStream_t s, size_t bytes, cudaMemPool_
 void scratch_cache_release(int slot, cudaStream_t s) {
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     CachedScratch& e = g_scratch[slot];
-    if (cudaEventRecord(e.last_use, s) != cudaSuccess) cudaGetLastError();
+    if (cudaEventRecord(e.last_use, s) == cudaSuccess) {
+        e.recorded = true;
+    } else {
+        cudaGetLastError();
+        e.recorded = false;  // its stream's later uses stay ordered; only eviction is barred
+    }
     e.busy = false;
     e.tick = ++g_scratch_tick;
 }
