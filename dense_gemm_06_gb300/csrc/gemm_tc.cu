@@ -227,7 +227,12 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, const TcLaunch& o,
     tp.tiles_m = (int)((pr.M + tile_m - 1) / tile_m);
     tp.tiles_n = (int)((pr.N + shape.tile_n - 1) / shape.tile_n);
     tp.split_mode = o.split_mode;  // the split itself is planned at launch (resident clusters)
-    tp.pdl = o.after_repack;
+    // Every launch is a programmatic dependent of what precedes it on the
+    // stream: the kernel waits (griddepcontrol.wait) before its first access
+    // to global memory, so an earlier kernel's writes are visible, while its
+    // launch and prologue overlap that kernel's tail when the earlier kernel
+    // signals its dependents (the repack and this kernel do so at their start).
+    tp.pdl = 1;
     tp.num_kb = (int)((pr.K + BK - 1) / BK);
     tp.c_vec = ((reinterpret_cast<uintptr_t>(pr.C) & 15u) == 0 &&
                 ((pr.ldc * out_bytes) & 15) == 0) ? 1 : 0;
@@ -262,7 +267,7 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, const TcLaunch& o,
                      tp.split_from, tp.clc ? "cluster-launch-control" : "persistent static",
                      a_mn ? "MN-major" : "K-major", b_mn ? "MN-major" : "K-major",
                      tp.c_tma ? "TMA stores" : "st.global", mc ? ", B multicast over two pairs" : "",
-                     tp.pdl ? ", waits on the repack (programmatic launch)" : "");
+                     o.after_repack ? ", waits on the repack (programmatic launch)" : "");
     }
     return rc;
 }

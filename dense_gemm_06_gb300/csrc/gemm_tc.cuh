@@ -36,7 +36,7 @@ struct TcParams {
                                // units (== tiles_m * tiles_n: none)
     int split_mode;            // host only: GEMM_OPT_TC_SPLIT_TAIL, resolved at launch
     int pdl;                   // host only: launched as a programmatic dependent of the
-                               // repack kernel before it on the stream
+                               // kernel before it on the stream
     int c_vec;                 // C base / ldc allow 16-byte stores
     ErrWord* err;              // device error word
     ErrWord gen;               // this launch's generation (see internal.h)
@@ -416,6 +416,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) TC_TRACE(p, 0);
+    // The next launch on the stream may set itself up meanwhile; it waits
+    // for this grid to complete before it touches global memory.
+    pdl_launch_dependents();
     const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;  // rank in the cluster
     const uint32_t rank = crank & (uint32_t)(CG - 1);          // rank in the CTA pair
     const int pair = MC ? (int)(crank >> 1) : 0;               // pair in the cluster

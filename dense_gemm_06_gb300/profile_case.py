@@ -6,6 +6,7 @@
     python -m dense_gemm_06_gb300.profile_case --case f16small --reps 3
     python -m dense_gemm_06_gb300.profile_case --case every
     python -m dense_gemm_06_gb300.profile_case --case bf16 --vendor --reps 2
+    python -m dense_gemm_06_gb300.profile_case --case f16skinny --dtype 3 --bm 0 --vendor --reps 2
 
 --case every runs one small call of each kernel of the library (for a
 launch list that covers all of them): the tcgen05 GEMM at its small and
@@ -127,6 +128,7 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=None, help="override M = N = K")
     ap.add_argument("--shape", type=int, nargs=3, metavar=("M", "N", "K"), default=None,
                     help="override M, N and K")
+    ap.add_argument("--dtype", type=int, default=None, help="override the GEMM_* data type")
     ap.add_argument("--am", type=int, default=None)
     ap.add_argument("--bm", type=int, default=None)
     ap.add_argument("--cta-group", type=int, default=0)
@@ -147,6 +149,7 @@ def main(argv=None):
         M = N = K = a.n
     if a.shape:
         M, N, K = a.shape
+    dtype = dtype if a.dtype is None else a.dtype
     am = am if a.am is None else a.am
     bm = bm if a.bm is None else a.bm
     it, ot = lg.IN_TYPE[dtype], lg.OUT_TYPE[dtype]
