@@ -58,8 +58,8 @@ OUT_TYPE = {GEMM_F32: "f32", GEMM_F16_F32: "f32", GEMM_BF16_F32: "f32",
             GEMM_F16_F16: "f16", GEMM_BF16_BF16: "bf16"}
 
 EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_noalloc", "gemm_tune", "gemm_tune_reset",
-           "softmax_rows", "gemm_strerror", "gemm_check_device_error", "gemm_release_workspace",
-           "gemm_launch_count", "gemm_set_option", "gemm_get_option")
+           "softmax_rows", "gemm_strerror", "gemm_check_device_error", "gemm_device_checks",
+           "gemm_release_workspace", "gemm_launch_count", "gemm_set_option", "gemm_get_option")
 
 _lock = threading.Lock()
 _lib = None
@@ -97,6 +97,8 @@ def load(path: str = LIB_PATH):
         lib.gemm_strerror.restype, lib.gemm_strerror.argtypes = ctypes.c_char_p, [ci]
         lib.gemm_check_device_error.restype = ci
         lib.gemm_check_device_error.argtypes = [vp]
+        lib.gemm_device_checks.restype = ci
+        lib.gemm_device_checks.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
         lib.gemm_release_workspace.restype, lib.gemm_release_workspace.argtypes = None, []
         lib.gemm_launch_count.restype, lib.gemm_launch_count.argtypes = ctypes.c_uint64, []
         lib.gemm_set_option.restype, lib.gemm_set_option.argtypes = ci, [ci, i64]
@@ -185,6 +187,14 @@ def gemm_strerror(status: int) -> str:
 
 def gemm_check_device_error(stream=None) -> int:
     return load().gemm_check_device_error(_stream(stream))
+
+
+def gemm_device_checks(stream=None):
+    """(status, first failed device-side check or 0); GEMM_ERR_UNSUPPORTED in a
+    library built without the checks."""
+    first = ctypes.c_uint64(0)
+    rc = load().gemm_device_checks(_stream(stream), ctypes.byref(first))
+    return rc, int(first.value)
 
 
 def gemm_release_workspace() -> None:

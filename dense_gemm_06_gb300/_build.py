@@ -4,6 +4,11 @@ Each translation unit compiles in parallel into _build/, with the ptxas
 resource report (registers, spills, shared memory) kept beside each object;
 the objects link into dense_gemm_06_gb300/libgemm.so against the shared CUDA
 runtime (so the library shares the runtime PyTorch already loaded).
+
+build(checks=True) compiles the debug build with device-side checks
+(-DLIBGEMM_DEVICE_CHECKS: tile coordinates, TMA coordinates and store
+addresses checked in the kernels, see gemm_device_checks in gemm.h) into
+_build_checks/ and libgemm_checks.so; the default build has none.
 """
 
 from __future__ import annotations
@@ -18,6 +23,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgemm.so")
+BUILD_CHECKS = os.path.join(HERE, "_build_checks")
+LIB_CHECKS = os.path.join(HERE, "libgemm_checks.so")
+CHECKS_FLAGS = ["-DLIBGEMM_DEVICE_CHECKS"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -46,13 +54,13 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def _compile(src: str, force: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, force: bool, out_dir: str = BUILD, extra=()) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
     log = obj[:-2] + ".ptxas.txt"
     if not force and os.path.exists(obj) and \
             os.path.getmtime(obj) >= max(os.path.getmtime(src), _deps_mtime()):
         return obj
-    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj + ".tmp"]
+    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj + ".tmp"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     with open(log, "w") as f:
         f.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
@@ -62,22 +70,25 @@ def _compile(src: str, force: bool) -> str:
     return obj
 
 
-def build(force: bool = False, jobs: int | None = None) -> str:
-    """Compile every csrc/*.cu for sm_103a and link libgemm.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, jobs: int | None = None, checks: bool = False) -> str:
+    """Compile every csrc/*.cu for sm_103a and link libgemm.so (checks: the
+    debug build with device-side checks, libgemm_checks.so); returns its path."""
+    out_dir, lib = (BUILD_CHECKS, LIB_CHECKS) if checks else (BUILD, LIB)
+    extra = CHECKS_FLAGS if checks else []
+    os.makedirs(out_dir, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, force), srcs))
+        objs = list(ex.map(lambda s: _compile(s, force, out_dir, extra), srcs))
     newest = max(os.path.getmtime(o) for o in objs)
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < newest:
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath," + _cuda_lib_dir()]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stderr[-6000:]}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 def ptxas_report() -> str:

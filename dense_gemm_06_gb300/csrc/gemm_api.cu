@@ -35,6 +35,7 @@ constexpr int kMaxDevices = 64;
 // Per-device error word written by kernels that give up on a wait (the
 // largest generation of a launch whose wait ran out; see internal.h).
 __device__ ErrWord g_err_word;
+__device__ unsigned long long g_check_word;  // first failed device-side check (debug build)
 std::atomic<ErrWord> g_generation{1};
 
 std::atomic<uint64_t> g_launches{0};
@@ -143,6 +144,10 @@ int current_device(DeviceInfo** out, cudaMemPool_t* pool) {
         st.info.cc_major = prop.major;
         st.info.cc_minor = prop.minor;
         st.info.err_word = static_cast<ErrWord*>(err);
+        if (check_word_address(&st.info.check_word) != kOk) {
+            st.status = kCuda;
+            return;
+        }
         if (cudaStreamCreateWithFlags(&st.h2d, cudaStreamNonBlocking) != cudaSuccess ||
             cudaStreamCreateWithFlags(&st.d2h, cudaStreamNonBlocking) != cudaSuccess) {
             cudaGetLastError();
@@ -362,6 +367,29 @@ int scratch_cache_acquire(int device, cudaStream_t s, size_t bytes, cudaMemPool_
     }
     e.busy = true;
     return slot;
+}
+
+// Frees every idle cached buffer (after the caller has synchronised the
+// devices; entries in use by a call are kept).
+void scratch_cache_clear() {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    for (CachedScratch& e : g_scratch) {
+        if (e.busy || e.device < 0) continue;
+        if (cudaSetDevice(e.device) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (e.ptr) cudaFree(e.ptr);
+        if (e.last_use) cudaEventDestroy(e.last_use);
+        e = CachedScratch{};
+    }
+    cudaSetDevice(cur);
+    cudaGetLastError();
 }
 
 void scratch_cache_release(int slot, cudaStream_t s) {
@@ -600,6 +628,16 @@ int error_word_address(ErrWord** out) {
         return kCuda;
     }
     *out = static_cast<ErrWord*>(p);
+    return kOk;
+}
+
+int check_word_address(unsigned long long** out) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_check_word) != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    *out = static_cast<unsigned long long*>(p);
     return kOk;
 }
 
@@ -1039,6 +1077,38 @@ int gemm_check_device_error(void* stream) {
     return kTimeout;
 }
 
+int gemm_device_checks(void* stream, uint64_t* first) {
+    if (!first) return kInvalidArg;
+    *first = 0;
+#ifndef LIBGEMM_DEVICE_CHECKS
+    (void)stream;
+    return kUnsupported;
+#else
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev, nullptr);
+    if (rc != kOk) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    unsigned long long word = 0;
+    if (cudaMemcpy(&word, dev->check_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    if (word != 0) {
+        const unsigned long long zero = 0;
+        if (cudaMemcpy(dev->check_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return kCuda;
+        }
+    }
+    *first = word;
+    return kOk;
+#endif
+}
+
 void gemm_release_workspace(void) {
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) {
@@ -1049,6 +1119,12 @@ void gemm_release_workspace(void) {
         if (!g_dev[d].pool) continue;
         if (cudaSetDevice(d) != cudaSuccess) { cudaGetLastError(); continue; }
         cudaDeviceSynchronize();
+    }
+    cudaSetDevice(cur);
+    scratch_cache_clear();  // the per-stream buffers go back to the pools
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (!g_dev[d].pool) continue;
+        if (cudaSetDevice(d) != cudaSuccess) { cudaGetLastError(); continue; }
         cudaMemPoolTrimTo(g_dev[d].pool, 0);
     }
     cudaSetDevice(cur);

@@ -79,6 +79,10 @@ int fixed_device(FixedDevice** out) {
         st.info.cc_major = major;
         st.info.cc_minor = minor;
         st.info.err_word = err;
+        if (check_word_address(&st.info.check_word) != kOk) {
+            st.status = kCuda;
+            return;
+        }
         st.status = kOk;
     });
     if (st.status != kOk) return st.status;

@@ -237,6 +237,7 @@ int launch_gemm_tc(const Problem& pr, const DeviceInfo& dev, const TcLaunch& o,
     tp.c_vec = ((reinterpret_cast<uintptr_t>(pr.C) & 15u) == 0 &&
                 ((pr.ldc * out_bytes) & 15) == 0) ? 1 : 0;
     tp.err = dev.err_word;
+    tp.check = dev.check_word;
     tp.gen = next_generation();
     tp.wait_limit_ns = o.wait_limit_ns;
     tp.fault_inject = o.fault_inject;

@@ -39,6 +39,7 @@ struct TcParams {
                                // kernel before it on the stream
     int c_vec;                 // C base / ldc allow 16-byte stores
     ErrWord* err;              // device error word
+    unsigned long long* check; // device-check word (debug build; see internal.h)
     ErrWord gen;               // this launch's generation (see internal.h)
     unsigned long long wait_limit_ns;
     int fault_inject;          // test hook: 1 = epilogue waits on a barrier nobody arrives at
@@ -178,6 +179,13 @@ __device__ __noinline__ void grace_period_ns(uint64_t ns) {
     }
 }
 
+// Debug build: true when element (row, col) lies inside C, else records the
+// failed check; always true in the default build.
+__device__ __forceinline__ bool c_inside(const TcParams& p, int row, int col) {
+    return device_check(p.check, row >= 0 && row < p.M && col >= 0 && col < p.N, kCheckTcStore,
+                        ((unsigned long long)(uint32_t)row << 24) | (uint32_t)col);
+}
+
 // Shared-memory helpers for the epilogue staging tile.
 __device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(a), "r"(x), "r"(y), "r"(z),
@@ -237,6 +245,7 @@ __device__ __forceinline__ void store_chunk_epi(const TcParams& p, uint32_t stag
         if (grow >= p.M) continue;
         OutT* dst = static_cast<OutT*>(p.C) + (int64_t)grow * p.ldc + gcol;
         if (p.c_vec && gcol + 3 < p.N) {
+            if (!c_inside(p, grow, gcol + 3)) continue;
             float old[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (sizeof(OutT) == 4) {
                 if (p.epi.beta != 0.f) {
@@ -266,7 +275,7 @@ __device__ __forceinline__ void store_chunk_epi(const TcParams& p, uint32_t stag
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (gcol + e >= p.N) continue;
+                if (gcol + e >= p.N || !c_inside(p, grow, gcol + e)) continue;
                 const float old = p.epi.beta != 0.f ? to_f32(dst[e]) : 0.f;
                 dst[e] = from_f32<OutT>(epilogue_value<OutT>(p.epi, f[e], old, grow, gcol + e));
             }
@@ -321,7 +330,9 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
     }
     // TMA only for chunks entirely inside C; edge chunks take the st.global
     // path below, so no store ever relies on clipping at the edges of C.
-    if (p.c_tma && row0 + 32 <= p.M && col0 + 32 <= p.N) {
+    if (p.c_tma && row0 + 32 <= p.M && col0 + 32 <= p.N &&
+        device_check(p.check, (col0 * ES) % 16 == 0 && row0 >= 0, kCheckTcTmaX,
+                     (unsigned long long)(uint32_t)col0)) {
         fence_proxy_async_smem();  // make the tile visible to the TMA engine
         __syncwarp();
         if (lane == 0) {
@@ -346,7 +357,8 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
             const int r = j * ROWS_PER_PASS + lane / UNITS;
             const uint4 val =
                 lds128(stage + (uint32_t)(r * ROW_BYTES) + (uint32_t)((u ^ swz<ES>(r)) * 16));
-            if (r < rows) *reinterpret_cast<uint4*>(dst) = val;
+            if (r < rows && c_inside(p, row0 + r, col0 + u * PER_UNIT + PER_UNIT - 1))
+                *reinterpret_cast<uint4*>(dst) = val;
             dst += ROWS_PER_PASS * step;
         }
     } else {
@@ -373,7 +385,7 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, uint32_t stage, i
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                if (rb + i < rows && col_ok) {
+                if (rb + i < rows && col_ok && c_inside(p, row0 + rb + i, col)) {
                     if constexpr (ES == 4) *reinterpret_cast<uint32_t*>(dst) = val[i];
                     else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)val[i];
                 }
@@ -450,6 +462,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         un.tm = MC ? tc.tm * 2 + pair : tc.tm;  // MC: may be past the last tile row (all OOB)
         un.col0 = tc.tn * p.tile_n + off;
         un.width = w;
+        device_check(p.check,
+                     un.tm >= 0 && un.tm < (MC ? 2 * unit_rows : p.tiles_m) && un.col0 >= 0 &&
+                         un.col0 % 64 == 0 && un.col0 + un.width <= p.tiles_n * p.tile_n,
+                     kCheckTcUnit, (unsigned long long)u);
         return un;
     };
     // Next unit of a role (t = total_units: no more work). Static schedule:
@@ -533,7 +549,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                     const uint32_t sa = sA0 + stage * C_::A_BYTES;
                     const uint32_t sb = sB0 + stage * C_::B_BYTES;
                     const int k0 = kb * BK;
-                    if (elect_one()) {
+                    // every innermost TMA coordinate below is k0, a_row + 64 j or
+                    // b_row + 64 j: 16-byte aligned when all three are multiples of 8
+                    const bool x_ok = device_check(p.check, ((k0 | a_row | b_row) & 7) == 0,
+                                                   kCheckTcTmaX, (unsigned long long)k0);
+                    if (x_ok && elect_one()) {
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes);
                     if (kb == 0 && t == cluster) TC_TRACE(p, 2);
                     if constexpr (!A_MN) {

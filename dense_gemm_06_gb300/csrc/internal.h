@@ -46,12 +46,40 @@ struct DeviceInfo {
     int sm_count;
     int cc_major, cc_minor;
     ErrWord* err_word;  // device address of this device's error word
+    unsigned long long* check_word;  // device address of its device-check word
+};
+
+// Device-side checks of the debug build (-DLIBGEMM_DEVICE_CHECKS): tile
+// coordinates, TMA coordinates and store addresses are checked in the
+// kernels; a failed check records (code << 56 | detail) in the device's check
+// word (the first failure wins) and the checked access is skipped. Without
+// the flag the checks compile to nothing. gemm_device_checks() reads and
+// clears the word.
+enum DeviceCheckCode : unsigned {
+    kCheckTcUnit = 1,      // tcgen05 work unit outside the tile grid (detail: unit)
+    kCheckTcTmaX = 2,      // a TMA copy's innermost coordinate not 16-byte aligned
+    kCheckTcStore = 3,     // an epilogue store outside C (detail: row << 24 | column)
+    kCheckSgTile = 4,      // FFMA tile or K-slice outside the problem (detail: CTA)
+    kCheckSgStore = 5,     // an FFMA store outside C (detail: row << 24 | column)
 };
 
 // A fresh launch generation (process-wide counter, starts at 1).
 ErrWord next_generation();
 
 #ifdef __CUDACC__
+// Debug build: records a failed check (see DeviceCheckCode); returns `ok`.
+__device__ __forceinline__ bool device_check(unsigned long long* word, bool ok, unsigned code,
+                                             unsigned long long detail) {
+#ifdef LIBGEMM_DEVICE_CHECKS
+    if (!ok && word)
+        atomicCAS(word, 0ull, ((unsigned long long)code << 56) | (detail & ((1ull << 56) - 1)));
+    return ok;
+#else
+    (void)word; (void)code; (void)detail;
+    return true;
+#endif
+}
+
 // True when a wait of the launch with generation `gen` has run out.
 __device__ __forceinline__ bool gen_failed(const ErrWord* err, ErrWord gen) {
     return *reinterpret_cast<const volatile ErrWord*>(err) == gen;
@@ -64,8 +92,7 @@ __device__ __forceinline__ void gen_record_timeout(ErrWord* err, ErrWord gen) {
 
 // Launchers return 0 or a gemm_status. They enqueue exactly the kernels they
 // report through note_launch().
-// Stream-ordered scratch for one launch sequence: get() allocates once from
-// the pool; the caller frees `ptr` on the stream after the launches.
+
 // Device scratch of one call, enqueued on `stream`: get() returns the
 // buffer (its first call sizes it), release() ends the call's use of it.
 // Buffers up to 64 MB come from a per-(device, stream) cache that keeps them
@@ -140,6 +167,8 @@ Problem normalised(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
                    const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int c_major,
                    int dtype);
 int error_word_address(ErrWord** out);
+// Device address of the current device's device-check word (debug build).
+int check_word_address(unsigned long long** out);
 // kOk when every non-null pointer of ptrs[0..n) is device memory of device
 // `device` (cudaPointerGetAttributes: type device, same ordinal), else
 // kInvalidArg. Host, managed and peer-device pointers are rejected before any

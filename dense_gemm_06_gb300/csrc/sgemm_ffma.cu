@@ -131,6 +131,7 @@ int launch_sgemm_f32(const Problem& pr, const DeviceInfo& dev, int config, int s
     sp.splits = 1;
     sp.kt_slice = 0;
     sp.ws = nullptr;
+    sp.check = dev.check_word;
     if ((int64_t)sp.tiles_m * sp.tiles_n > 0x3fffffffLL) return kUnsupported;
 
     // A/B variant: K-major (4-byte transposing copies), MN-major 16-byte or 4-byte.

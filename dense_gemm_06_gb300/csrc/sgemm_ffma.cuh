@@ -25,6 +25,7 @@ struct SgemmParams {
     int splits;     // K-slices of each later tile (one CTA per slice)
     int kt_slice;   // k-tiles per slice
     float* ws;      // raw partial tiles of the slices: [unit][128 * 128 / 4] float4
+    unsigned long long* check;  // device-check word (debug build; see internal.h)
 };
 
 // Launches configuration N (1..8, as GEMM_OPT_SIMT_CONFIG numbers them) for
@@ -114,6 +115,23 @@ __device__ __forceinline__ void thread_block(int tid, int& ty, int& tx) {
     }
 }
 
+// Debug build: true when element (row, col) lies inside C, else records the
+// failed check; always true in the default build.
+__device__ __forceinline__ bool sg_inside(const SgemmParams& p, int row, int col) {
+    return device_check(p.check, row >= 0 && row < p.M && col >= 0 && col < p.N, kCheckSgStore,
+                        ((unsigned long long)(uint32_t)row << 24) | (uint32_t)col);
+}
+
+// Debug build: checks a CTA's tile origin and K-slice (kt0 .. kt0 + nkt of
+// total k-tiles) against the problem.
+__device__ __forceinline__ void sg_check_tile(const SgemmParams& p, int m0, int n0, int kt0,
+                                              int nkt, int total) {
+    device_check(p.check,
+                 m0 >= 0 && m0 < p.M && n0 >= 0 && n0 < p.N && kt0 >= 0 && nkt >= 0 &&
+                     kt0 + nkt <= total,
+                 kCheckSgTile, (unsigned long long)blockIdx.x);
+}
+
 // Stores the thread's 8 x TN block of the tile at (m0, n0), applying the
 // fused epilogue when one is active; predicated on M and N.
 template <int TN>
@@ -147,11 +165,12 @@ __device__ __forceinline__ void store_block(const SgemmParams& p, const float2 (
                     if (col + j < p.N) v[j] = epilogue_value<float>(p.epi, v[j], old[j], row, col + j);
             }
             if (p.c_vec && col + 3 < p.N) {
-                *reinterpret_cast<float4*>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
+                if (sg_inside(p, row, col + 3))
+                    *reinterpret_cast<float4*>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (col + j < p.N) crow[col + j] = v[j];
+                    if (col + j < p.N && sg_inside(p, row, col + j)) crow[col + j] = v[j];
             }
         }
     }
@@ -286,6 +305,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) sgemm_ffma_kernel(con
     }
     int m0, n0, ty, tx;
     tile_origin(p, t, m0, n0);
+    sg_check_tile(p, m0, n0, kt0, nkt, (p.K + BK - 1) / BK);
     thread_block<TN>(tid, ty, tx);
 
     const uint32_t s0 = smem_addr(smem);
@@ -385,6 +405,7 @@ __global__ void __launch_bounds__(BM * BN / (8 * TN)) sgemm_split_fixup_kernel(
     const int tid = threadIdx.x;
     int m0, n0, ty, tx;
     tile_origin(p, p.dp_tiles + blockIdx.x, m0, n0);
+    sg_check_tile(p, m0, n0, 0, 0, 0);
     thread_block<TN>(tid, ty, tx);
     const float4* wsp = reinterpret_cast<const float4*>(p.ws) +
                         (size_t)blockIdx.x * p.splits * (BM * BN / 4) + tid;

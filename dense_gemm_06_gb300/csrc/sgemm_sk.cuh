@@ -127,6 +127,8 @@ __global__ void __launch_bounds__(TC::Cfg::THREADS, TC::Cfg::MINB)
     // which waits for it), then the part of tile t
     int mh = 0, nh = 0;
     if (n_head > 0) tile_origin(p, t + 1, mh, nh);
+    sg_check_tile(p, m0, n0, kt0, nkt - n_head, nkt_tile);
+    if (n_head > 0) sg_check_tile(p, mh, nh, 0, n_head, nkt_tile);
 
     if (tid == 0) {
         tma_prefetch_desc(&tmap_a);

@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(TC::Cfg::THREADS, TC::Cfg::MINB)
     }
     int m0, n0, ty, tx;
     tile_origin(p, t, m0, n0);
+    sg_check_tile(p, m0, n0, kt0, nkt, (p.K + kTmaBK - 1) / kTmaBK);
     thread_block<TN>(tid, ty, tx);
 
     if (tid == 0) {

@@ -270,10 +270,24 @@ const char *gemm_strerror(int status);
 int gemm_check_device_error(void *stream);
 
 /*
+ * gemm_device_checks -- debug builds only (the library compiled with
+ * LIBGEMM_DEVICE_CHECKS): synchronises `stream`, then reads and clears the
+ * current device's device-check word into *first: 0 when every device-side
+ * check passed since the last call, else (code << 56 | detail) of the first
+ * that failed (codes: 1 a tensor-core work unit outside the tile grid, 2 a
+ * TMA coordinate not 16-byte aligned, 3 a tensor-core epilogue store outside
+ * C, 4 an FFMA tile or K-slice outside the problem, 5 an FFMA store outside
+ * C); the failed access itself was skipped. Returns GEMM_OK, GEMM_ERR_CUDA,
+ * GEMM_ERR_INVALID_ARG (first == NULL), or GEMM_ERR_UNSUPPORTED in a library
+ * built without the checks (*first = 0).
+ */
+int gemm_device_checks(void *stream, uint64_t *first);
+
+/*
  * gemm_release_workspace -- synchronises every device the library has used
- * and returns the cached scratch memory of its pools (repack buffers and
- * gemm_host() copies) to the driver. Call it when no other thread is inside a
- * gemm* call.
+ * and returns its cached scratch memory (the per-stream repack and split
+ * buffers, and what its pools keep of repack buffers and gemm_host() copies)
+ * to the driver. Call it when no other thread is inside a gemm* call.
  */
 void gemm_release_workspace(void);
 

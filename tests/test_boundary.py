@@ -199,3 +199,10 @@ def test_missing_library_fails_loudly(tmp_path):
             mod.load(str(tmp_path / "libgemm.so"))
         finally:
             mod._lib = saved
+
+
+def test_device_checks_absent_from_the_default_build(lib):
+    # gemm_device_checks answers only in the debug build with device-side
+    # checks; the default library says so without touching a device
+    rc, first = lg.gemm_device_checks()
+    assert rc == lg.GEMM_ERR_UNSUPPORTED and first == 0
