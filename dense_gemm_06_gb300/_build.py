@@ -8,7 +8,11 @@ runtime (so the library shares the runtime PyTorch already loaded).
 build(checks=True) compiles the debug build with device-side checks
 (-DLIBGEMM_DEVICE_CHECKS: tile coordinates, TMA coordinates and store
 addresses checked in the kernels, see gemm_device_checks in gemm.h) into
-_build_checks/ and libgemm_checks.so; the default build has none.
+_build_checks/ and libgemm_checks.so; build(trace=True) the phase-trace
+build of the tensor-core kernel (-DLIBGEMM_TC_TRACE: %globaltimer stamps at
+fixed points of every role, 64 per CTA, into a device buffer registered with
+the extra export libgemm_tc_trace_buffer(void*)) into _build_trace/ and
+libgemm_trace.so. The default build has neither.
 """
 
 from __future__ import annotations
@@ -26,6 +30,9 @@ LIB = os.path.join(HERE, "libgemm.so")
 BUILD_CHECKS = os.path.join(HERE, "_build_checks")
 LIB_CHECKS = os.path.join(HERE, "libgemm_checks.so")
 CHECKS_FLAGS = ["-DLIBGEMM_DEVICE_CHECKS"]
+BUILD_TRACE = os.path.join(HERE, "_build_trace")
+LIB_TRACE = os.path.join(HERE, "libgemm_trace.so")
+TRACE_FLAGS = ["-DLIBGEMM_TC_TRACE"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -70,11 +77,18 @@ def _compile(src: str, force: bool, out_dir: str = BUILD, extra=()) -> str:
     return obj
 
 
-def build(force: bool = False, jobs: int | None = None, checks: bool = False) -> str:
+def build(force: bool = False, jobs: int | None = None, checks: bool = False,
+          trace: bool = False) -> str:
     """Compile every csrc/*.cu for sm_103a and link libgemm.so (checks: the
-    debug build with device-side checks, libgemm_checks.so); returns its path."""
-    out_dir, lib = (BUILD_CHECKS, LIB_CHECKS) if checks else (BUILD, LIB)
-    extra = CHECKS_FLAGS if checks else []
+    debug build with device-side checks, libgemm_checks.so; trace: the
+    phase-trace build, libgemm_trace.so); returns its path."""
+    if checks and trace:
+        raise ValueError("one debug variant at a time")
+    out_dir, lib, extra = BUILD, LIB, []
+    if checks:
+        out_dir, lib, extra = BUILD_CHECKS, LIB_CHECKS, CHECKS_FLAGS
+    elif trace:
+        out_dir, lib, extra = BUILD_TRACE, LIB_TRACE, TRACE_FLAGS
     os.makedirs(out_dir, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
