@@ -554,34 +554,39 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                     const bool x_ok = device_check(p.check, ((k0 | a_row | b_row) & 7) == 0,
                                                    kCheckTcTmaX, (unsigned long long)k0);
                     if (x_ok && elect_one()) {
-                    if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes);
-                    if (kb == 0 && t == cluster) TC_TRACE(p, 2);
-                    if constexpr (!A_MN) {
-                        tma_load_2d<CG>(sa, &p.tmap_a, fb, k0, a_row);
-                    } else {
+                        if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes);
+                        if (kb == 0 && t == cluster) TC_TRACE(p, 2);
+                        if constexpr (!A_MN) {
+                            tma_load_2d<CG>(sa, &p.tmap_a, fb, k0, a_row);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < ROWS_A / 64; ++j)
-                            tma_load_2d<CG>(sa + j * 64 * BK * 2, &p.tmap_a, fb, a_row + 64 * j, k0);
-                    }
-                    if constexpr (MC) {
-                        // this pair's 64-row piece of B-half `rank`, to both pairs
-                        const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
-                        const uint32_t dst = sb + (uint32_t)(pair * 64 * BK * 2);
-                        if constexpr (!B_MN)
-                            tma_load_2d_mc_pair(dst, &p.tmap_b, fb, k0, b_row + 64 * pair, mask);
-                        else
-                            tma_load_2d_mc_pair(dst, &p.tmap_b, fb, b_row + 64 * pair, k0, mask);
-                    } else if constexpr (!B_MN) {
-                        // the CTA's rows of B in one box (fewer, larger boxes
-                        // measured faster: two 64-row boxes cost 4% at 8192^3)
-                        tma_load_2d<CG>(sb, un.width == p.tile_n ? &p.tmap_b : &p.tmap_b_half,
-                                        fb, k0, b_row);
-                    } else {
-                        // 64-column boxes (the width of the 128-byte swizzle)
-                        for (int j = 0; j < b_rows / 64; ++j)
-                            tma_load_2d<CG>(sb + j * 64 * BK * 2, &p.tmap_b, fb,
-                                            b_row + 64 * j, k0);
-                    }
+                            for (int j = 0; j < ROWS_A / 64; ++j)
+                                tma_load_2d<CG>(sa + j * 64 * BK * 2, &p.tmap_a, fb,
+                                                a_row + 64 * j, k0);
+                        }
+                        if constexpr (MC) {
+                            // this pair's 64-row piece of B-half `rank`, to both pairs
+                            const uint16_t mask =
+                                (uint16_t)((1u << rank) | (1u << (rank + 2)));
+                            const uint32_t dst = sb + (uint32_t)(pair * 64 * BK * 2);
+                            if constexpr (!B_MN)
+                                tma_load_2d_mc_pair(dst, &p.tmap_b, fb, k0, b_row + 64 * pair,
+                                                    mask);
+                            else
+                                tma_load_2d_mc_pair(dst, &p.tmap_b, fb, b_row + 64 * pair, k0,
+                                                    mask);
+                        } else if constexpr (!B_MN) {
+                            // the CTA's rows of B in one box (fewer, larger boxes
+                            // measured faster: two 64-row boxes cost 4% at 8192^3)
+                            tma_load_2d<CG>(sb,
+                                            un.width == p.tile_n ? &p.tmap_b : &p.tmap_b_half,
+                                            fb, k0, b_row);
+                        } else {
+                            // 64-column boxes (the width of the 128-byte swizzle)
+                            for (int j = 0; j < b_rows / 64; ++j)
+                                tma_load_2d<CG>(sb + j * 64 * BK * 2, &p.tmap_b, fb,
+                                                b_row + 64 * j, k0);
+                        }
                     }
                     __syncwarp();
                     if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
@@ -631,12 +636,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                     const uint64_t bd = b_desc0 + (uint64_t)(stage * (C_::B_BYTES >> 4));
                     if (elect_one()) {
 #pragma unroll
-                    for (int j = 0; j < BK / UMMA_K; ++j)
-                        mma_f16<CG>(d_tmem, ad + (uint64_t)(j * (A_STEP >> 4)),
-                                    bd + (uint64_t)(j * (B_STEP >> 4)), idesc,
-                                    (kb | j) != 0 ? 1u : 0u);
-                    if constexpr (MC) mma_commit_pair(empty_bar(stage), (uint16_t)0xF);
-                    else mma_commit<CG>(empty_bar(stage));
+                        for (int j = 0; j < BK / UMMA_K; ++j)
+                            mma_f16<CG>(d_tmem, ad + (uint64_t)(j * (A_STEP >> 4)),
+                                        bd + (uint64_t)(j * (B_STEP >> 4)), idesc,
+                                        (kb | j) != 0 ? 1u : 0u);
+                        if constexpr (MC) mma_commit_pair(empty_bar(stage), (uint16_t)0xF);
+                        else mma_commit<CG>(empty_bar(stage));
                     }
                     __syncwarp();
                     if (++stage == C_::STAGES) { stage = 0; phase ^= 1u; }
