@@ -404,6 +404,7 @@ void scratch_cache_release(int slot, cudaStream_t s) {
     e.busy = false;
     e.tick = ++g_scratch_tick;
 }
+
 int run_sgemm(Problem p, const DeviceInfo& dev, cudaMemPool_t pool, const RunConfig& cfg,
               cudaStream_t s) {
     void* scratch[2] = {nullptr, nullptr};
