@@ -816,13 +816,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a
         const bool a_panels = np > 1;
         const int64_t prow = rows;
         // With an fp32 C the first panel is pipelined over K as well: B and
-        // that panel's A arrive in kp pieces of K, and the panel runs as kp
-        // GEMMs, each adding its product to C (fused epilogue, beta = 1), so
-        // its first GEMM starts once a kp-th of B is in instead of all of it.
-        // (A 16-bit C would be rounded between the pieces, so it goes whole.)
-        constexpr int kKp = 4;
-        const int kp = (np > 1 && oe == 4 && K >= kKp * 256) ? kKp : 1;
-        auto kbound = [&](int j) { return j == kp ? K : round_up(K * j / kp, 64); };
+        // that panel's A arrive in kp pieces of K and the panel runs as kp
+        // GEMMs accumulating into C (host_k_pieces / host_k_bound, policy.h).
+        const int kp = host_k_pieces(np, (int)oe, K);
+        auto kbound = [&](int j) { return host_k_bound(K, kp, j); };
         dispatch_log("gemm_host %lldx%lldx%lld: %d row panel(s) of %lld rows, the first in %d "
                      "piece(s) of K",
                      (long long)pd.M, (long long)pd.N, (long long)K, np, (long long)rows, kp);

@@ -117,6 +117,25 @@ inline bool want_transpose(int64_t other_dim, int64_t M, int64_t N, int64_t K, i
     return other_dim >= 512 && (double)M * (double)N * (double)K >= 2147483648.0;
 }
 
+// gemm_host(): with more than one row panel and an fp32 C, the first panel
+// runs as host_k_pieces() GEMMs over consecutive ranges of K, each adding its
+// product to C (fused epilogue, beta = 1), so the first one starts once a
+// quarter of B (and of that panel's A) is in instead of all of it. A 16-bit C
+// would be rounded between the pieces, and K below 4 x 256 would leave pieces
+// too short to pay for their launches: those run whole (1 piece).
+constexpr int kHostKPieces = 4;
+inline int host_k_pieces(int64_t panels, int out_bytes, int64_t K) {
+    return panels > 1 && out_bytes == 4 && K >= kHostKPieces * 256 ? kHostKPieces : 1;
+}
+
+// First k of piece j of `pieces` (j == pieces: K): K j / pieces rounded up to
+// a multiple of 64, so every piece but the last covers whole 64-deep k-tiles.
+inline int64_t host_k_bound(int64_t K, int pieces, int j) {
+    if (j >= pieces) return K;
+    const int64_t b = (K * j / pieces + 63) / 64 * 64;
+    return b < K ? b : K;
+}
+
 // Rows of the normalised C per gemm_host() panel: a whole number of waves of
 // the kernel that computes it (so no panel adds a partial wave), at most
 // about 8 panels; M itself when the product is too small (M N K < 1e10) for

@@ -8,6 +8,7 @@
 //   tcshape M N cta_group tile_n multicast sm_count         -> "cta_group tile_n"
 //   tcsplit T slots tile_n cta_group multicast mode          -> "split_from"
 //   sk T slots sm_count nkt mode                               -> "dp_tiles sk_ctas"
+//   kpieces panels out_bytes K                    -> "pieces bound_0 .. bound_pieces"
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -53,6 +54,14 @@ int main(int argc, char** argv) {
         const StreamK k = plan_stream_k(arg(argv, 2), (int)arg(argv, 3), (int)arg(argv, 4),
                                         (int)arg(argv, 5), (int)arg(argv, 6));
         std::printf("%d %d\n", k.dp_tiles, k.sk_ctas);
+        return 0;
+    }
+    if (argc >= 5 && std::strcmp(argv[1], "kpieces") == 0) {
+        const int n = host_k_pieces(arg(argv, 2), (int)arg(argv, 3), arg(argv, 4));
+        std::printf("%d", n);
+        for (int j = 0; j <= n; ++j)
+            std::printf(" %lld", (long long)host_k_bound(arg(argv, 4), n, j));
+        std::printf("\n");
         return 0;
     }
     std::fprintf(stderr, "usage: see the header of policy_probe.cc\n");

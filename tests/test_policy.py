@@ -169,3 +169,22 @@ def test_stream_k(probe):
     assert probe("sk", 30, SLOTS, P, 64, 3) == (10, 30)
     assert probe("sk", 7, SLOTS, P, 64, 3) == (2, 8)
     assert probe("sk", 4, SLOTS, P, 1, 3) == (1, 3)
+
+
+def test_host_k_pieces(probe):
+    # fp32 C with several panels: the first panel in 4 pieces of whole 64-deep
+    # k-tiles (the last piece takes the remainder)
+    assert probe("kpieces", 4, 4, 8192) == (4, 0, 2048, 4096, 6144, 8192)
+    assert probe("kpieces", 2, 4, 1037) == (4, 0, 320, 576, 832, 1037)
+    assert probe("kpieces", 2, 4, 1024) == (4, 0, 256, 512, 768, 1024)
+    # one panel, a 16-bit C (rounded between pieces), or K under 4 x 256: whole
+    assert probe("kpieces", 1, 4, 8192) == (1, 0, 8192)
+    assert probe("kpieces", 4, 2, 8192) == (1, 0, 8192)
+    assert probe("kpieces", 4, 4, 1023) == (1, 0, 1023)
+    # every K from 1024 up: bounds increase, every piece but the last is a
+    # whole number of 64-deep k-tiles, and the pieces cover [0, K)
+    for K in list(range(1024, 1300)) + [4095, 8191, 65537]:
+        n, *b = probe("kpieces", 3, 4, K)
+        assert n == 4 and b[0] == 0 and b[-1] == K
+        assert all(b[j] < b[j + 1] for j in range(n)), (K, b)
+        assert all(b[j] % 64 == 0 for j in range(n)), (K, b)
